@@ -1,0 +1,325 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself -- hand-derived closed forms, textbook/library routines (numpy matmul,
+argsort, scipy softmax/expit, torch's own fp32->bf16 rounding and rms_norm),
+invariants and brute force on tiny inputs -- so that a dropped term, a wrong
+sign or index, a swapped nibble or a transposed operand fails one of them."""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from quantised_expert_ffn_gb300 import synth
+from tests.util import bf16_f64, bits, oracle_layer
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_rounding_hand_cases(oracle_mod):
+    f = oracle_mod.f64_to_bf16
+    cases = {
+        1.0: 0x3F80,
+        -2.0: 0xC000,
+        1.0 + 2.0 ** -8: 0x3F80,                  # tie -> even (down)
+        1.0 + 3 * 2.0 ** -8: 0x3F82,              # tie -> even (up)
+        1.0 + 2.0 ** -8 + 2.0 ** -30: 0x3F81,     # just above the tie: one rounding, up
+        2.0 ** -130: 0x0008,                      # subnormal: 8 * 2^-133
+        3.5e38: 0x7F80,                           # overflow -> inf
+        0.0: 0x0000,
+    }
+    for v, b in cases.items():
+        assert int(f(v)) == b, (v, hex(int(f(v))), hex(b))
+
+
+def test_bf16_rounding_matches_torch_on_fp32(oracle_mod):
+    g = torch.Generator().manual_seed(5)
+    v = torch.randn(4000, generator=g) * torch.exp(torch.randn(4000, generator=g) * 8)
+    ours = oracle_mod.f64_to_bf16(v.double().numpy())
+    theirs = bits(v.to(torch.bfloat16))
+    assert np.array_equal(ours, theirs)
+
+
+def test_bf16_round_trip_all_finite(oracle_mod):
+    pats = np.arange(0, 65536, 97, dtype=np.uint32).astype(np.uint16)
+    vals = bf16_f64(pats)
+    keep = np.isfinite(vals)
+    back = oracle_mod.f64_to_bf16(vals[keep])
+    # +0/-0 both fine; everything else must come back bit-identical
+    assert np.array_equal(back, pats[keep])
+
+
+# ---------------------------------------------------------------- Q4 layout / dequant
+
+def _zero_layer(D=128, F=64, E=2, K=1, seed=0):
+    """A layer whose every weight is exactly 0 (codes 8, bias = -8 * scale)."""
+    W = synth.layer_weights(D, E, F, K, seed=seed)
+    for n in ("gate_q", "up_q", "down_q"):
+        getattr(W, n).fill_(0x88)
+    return W
+
+
+def test_zero_weights_give_identity(oracle_mod):
+    """q = 8 with bias = -8 s gives w = 0 exactly, so y = r bit-exactly."""
+    W = _zero_layer(K=2, E=4)
+    L = oracle_layer(W)
+    r = bits(synth.hidden(1, 128, seed=3))[0]
+    out = oracle_mod.moe_token(L, r)
+    assert np.array_equal(out["y_bf16"], r)
+    assert np.all(out["expert_out"] == 0.0)
+
+
+def _set_code(q, row, col, code):
+    byte = q[row, col // 2]
+    if col % 2 == 0:
+        q[row, col // 2] = (byte & 0xF0) | code
+    else:
+        q[row, col // 2] = (byte & 0x0F) | (code << 4)
+
+
+@pytest.mark.parametrize("d0,j0,d1", [(70, 5, 33), (71, 6, 32), (0, 0, 127), (127, 63, 1)])
+def test_single_code_pins_layout(oracle_mod, d0, j0, d1):
+    """One code moved off 8 in gate (row j0, col d0) and in down (row d1, col j0):
+    g is zero except g[j0] = s_g * x[d0]; o is zero except o[d1] = s_d * h[j0].
+    Distinct scales per group make a wrong group, nibble or transposition show."""
+    D, F = 128, 64
+    W = _zero_layer(D=D, F=F, E=1, K=1)
+    # distinct exact scales per (row, group), bias = -8 s keeps w = 0 elsewhere
+    gs = (torch.arange(F * D // 64, dtype=torch.float32).reshape(1, F, D // 64) + 1) / 256
+    W.gate_s = gs.to(torch.bfloat16)
+    W.gate_b = (W.gate_s.float() * -8).to(torch.bfloat16)
+    W.up_s = torch.zeros_like(W.up_s)
+    W.up_b = torch.full_like(W.up_b, 1 / 64)          # constant up matrix
+    ds = (torch.arange(D * F // 64, dtype=torch.float32).reshape(1, D, F // 64) + 3) / 512
+    W.down_s = ds.to(torch.bfloat16)
+    W.down_b = (W.down_s.float() * -8).to(torch.bfloat16)
+    _set_code(W.gate_q[0], j0, d0, 9)
+    _set_code(W.down_q[0], d1, j0, 11)
+    L = oracle_layer(W)
+    x = bits(synth.hidden(1, D, seed=11))[0]
+    xf = bf16_f64(x)
+    o, h = oracle_mod.expert_ffn(L, 0, x)
+    s_g = float(W.gate_s[0, j0, d0 // 64])
+    g = s_g * 1 * xf[d0]
+    u = xf.sum() / 64
+    hj = g * scipy.special.expit(g) * u
+    assert np.count_nonzero(h) == 1 and h[j0] == pytest.approx(hj, rel=1e-13)
+    s_d = float(W.down_s[0, d1, j0 // 64])
+    assert np.count_nonzero(o) == 1 and o[d1] == pytest.approx(3 * s_d * hj, rel=1e-13)
+
+
+def _numpy_dequant(q, s, b):
+    """Independent unpack of the documented Q4 layout with numpy."""
+    lo = (q & 0x0F).astype(np.float64)
+    hi = (q >> 4).astype(np.float64)
+    codes = np.stack([lo, hi], axis=-1).reshape(q.shape[0], -1)
+    return codes * np.repeat(bf16_f64(s), 64, axis=1) + np.repeat(bf16_f64(b), 64, axis=1)
+
+
+def test_expert_ffn_matches_numpy_matmul(oracle_mod):
+    """Brute force on a tiny layer: numpy fp64 matmul of the dequantised matrices."""
+    D, F, E = 128, 128, 3
+    W = synth.layer_weights(D, E, F, 2, seed=21)
+    # a general (not -8 s) bias, so that the affine term is exercised
+    W.gate_b = (torch.randn(W.gate_b.shape) * 0.01).to(torch.bfloat16)
+    W.down_b = (torch.randn(W.down_b.shape) * 0.01).to(torch.bfloat16)
+    L = oracle_layer(W)
+    x = bits(synth.hidden(1, D, seed=4))[0]
+    xf = bf16_f64(x)
+    for e in range(E):
+        Wg = _numpy_dequant(L.gate_q[e], L.gate_s[e], L.gate_b[e])
+        Wu = _numpy_dequant(L.up_q[e], L.up_s[e], L.up_b[e])
+        Wd = _numpy_dequant(L.down_q[e], L.down_s[e], L.down_b[e])
+        g, u = Wg @ xf, Wu @ xf
+        h_ref = g * scipy.special.expit(g) * u
+        o_ref = Wd @ h_ref
+        o, h = oracle_mod.expert_ffn(L, e, x)
+        np.testing.assert_allclose(h, h_ref, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-11, atol=1e-14)
+
+
+def test_silu_closed_forms(oracle_mod):
+    """Constant matrices reduce the FFN to scalars: g = cg * sum x, u = cu * sum x,
+    o = cd * F * SiLU(g) * u.  At g = 0 the output is 0; at large |g| SiLU is g or 0."""
+    D, F = 64, 64
+    x = np.full(D, 0x3F80, np.uint16)                 # ones: sum x = 64
+    for cg, expect in [(0.0, lambda g, u: 0.0),
+                       (0.5, lambda g, u: g * u),     # g = 32: sigma(32) = 1 - 1.3e-14
+                       (-0.5, lambda g, u: 0.0)]:     # g = -32: g*sigma(g) = -4e-13
+        W = synth.layer_weights(D, 1, F, 1, seed=1)
+        for n in ("gate_s", "up_s", "down_s"):
+            setattr(W, n, torch.zeros_like(getattr(W, n)))
+        W.gate_b = torch.full_like(W.gate_b, cg)
+        W.up_b = torch.full_like(W.up_b, 1 / 64)
+        W.down_b = torch.full_like(W.down_b, 1 / 64)
+        o, h = oracle_mod.expert_ffn(oracle_layer(W), 0, x)
+        g, u = 64 * cg, 1.0
+        np.testing.assert_allclose(h, expect(g, u), rtol=1e-12, atol=1e-11)
+        np.testing.assert_allclose(o, F / 64 * expect(g, u), rtol=1e-12, atol=1e-11)
+
+
+# ---------------------------------------------------------------- router, top-k, weights
+
+def test_router_logits_match_numpy(oracle_mod):
+    W = synth.layer_weights(256, 16, 64, 4, seed=8)
+    L = oracle_layer(W)
+    x = bits(synth.hidden(1, 256, seed=9))[0]
+    ref = bf16_f64(L.router_w) @ bf16_f64(x)
+    np.testing.assert_allclose(oracle_mod.router_logits(L, x), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_topk_matches_full_sort_with_ties(oracle_mod):
+    rng = np.random.default_rng(3)
+    for trial in range(50):
+        E = int(rng.integers(1, 160))
+        k = int(rng.integers(1, E + 1))
+        logits = np.round(rng.normal(size=E), 1)      # many exact ties
+        key32 = logits.astype(np.float32)
+        ref = np.lexsort((np.arange(E), -key32))[:k]
+        assert np.array_equal(oracle_mod.topk(logits, k), ref)
+
+
+def test_topk_k_equals_e_is_permutation(oracle_mod):
+    logits = np.random.default_rng(0).normal(size=33)
+    idx = oracle_mod.topk(logits, 33)
+    assert sorted(idx.tolist()) == list(range(33))
+    assert np.all(np.diff(logits[idx]) <= 0)
+
+
+def test_topk_decides_in_fp32(oracle_mod):
+    """Two logits that differ only below fp32 resolution tie; the lower id wins."""
+    logits = np.array([1.0, 1.0 + 2.0 ** -40, 0.5])
+    assert oracle_mod.topk(logits, 1)[0] == 0
+
+
+def test_mix_weights(oracle_mod):
+    rng = np.random.default_rng(1)
+    logits = rng.normal(size=128) * 2
+    idx = oracle_mod.topk(logits, 8)
+    w = oracle_mod.mix_weights(logits, idx, True)
+    assert abs(w.sum() - 1.0) < 8 * 2.0 ** -24
+    assert np.all(np.diff(w) <= 0)
+    np.testing.assert_allclose(w, scipy.special.softmax(logits[idx]), rtol=1e-13)
+    w_all = oracle_mod.mix_weights(logits, idx, False)
+    np.testing.assert_allclose(w_all, scipy.special.softmax(logits)[idx], rtol=1e-13)
+    full = oracle_mod.topk(logits, 128)
+    np.testing.assert_allclose(oracle_mod.mix_weights(logits, full, True),
+                               scipy.special.softmax(logits)[full], rtol=1e-13)
+
+
+def test_single_expert_layer(oracle_mod):
+    """E = 1, k = 1: w = 1 and y = r + FFN(r)."""
+    W = synth.layer_weights(64, 1, 64, 1, seed=2)
+    L = oracle_layer(W)
+    r = bits(synth.hidden(1, 64, seed=7))[0]
+    out = oracle_mod.moe_token(L, r)
+    assert out["idx"].tolist() == [0] and out["w"][0] == 1.0
+    o, _ = oracle_mod.expert_ffn(L, 0, r)
+    np.testing.assert_array_equal(out["y"], bf16_f64(r) + o)
+
+
+def test_rmsnorm_matches_torch(oracle_mod):
+    D = 256
+    W = synth.layer_weights(D, 4, 64, 2, seed=3, rms_norm=True)
+    W.rms_gain = (1 + 0.1 * torch.randn(D, generator=torch.Generator().manual_seed(1))).to(
+        torch.bfloat16)
+    L = oracle_layer(W)
+    r = synth.hidden(1, D, seed=12)[0] * 3
+    ref = torch.nn.functional.rms_norm(r.double(), (D,), W.rms_gain.double(), eps=1e-6)
+    assert np.array_equal(oracle_mod.rmsnorm(L, bits(r)), oracle_mod.f64_to_bf16(ref.numpy()))
+
+
+# ---------------------------------------------------------------- union and buckets
+
+def _brute_union(idx, E):
+    buckets = {}
+    for t, row in enumerate(idx):
+        for i, e in enumerate(row):
+            buckets.setdefault(int(e), []).append((t, i))
+    return buckets
+
+
+@pytest.mark.parametrize("T,k,E,seed", [(1, 8, 128, 0), (45, 8, 128, 1), (64, 8, 128, 2),
+                                        (7, 3, 5, 3), (64, 8, 16, 4)])
+def test_union_matches_python_dict(oracle_mod, T, k, E, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    u = oracle_mod.expert_union(idx, E)
+    ref = _brute_union(idx, E)
+    assert u["n_union"] == len(ref)
+    assert u["union_ids"][:u["n_union"]].tolist() == sorted(ref)
+    assert np.all(u["union_ids"][u["n_union"]:] == -1)
+    for n, e in enumerate(sorted(ref)):
+        lo, hi = u["offsets"][n], u["offsets"][n + 1]
+        got = list(zip(u["bucket_tok"][lo:hi].tolist(), u["bucket_rank"][lo:hi].tolist()))
+        assert got == ref[e]
+    assert np.all(u["offsets"][u["n_union"]:] == T * k)
+
+
+def test_union_degenerate_cases(oracle_mod):
+    same = np.tile(np.arange(8, dtype=np.int32)[::-1], (64, 1))
+    assert oracle_mod.expert_union(same, 128)["n_union"] == 8
+    distinct = np.arange(128, dtype=np.int32).reshape(16, 8)
+    assert oracle_mod.expert_union(distinct, 128)["n_union"] == 128
+    few = np.arange(24, dtype=np.int32).reshape(3, 8)
+    assert oracle_mod.expert_union(few, 128)["n_union"] == 24
+
+
+def test_union_skips_out_of_range(oracle_mod):
+    idx = np.array([[0, 5, 200], [-1, 5, 3]], np.int32)
+    u = oracle_mod.expert_union(idx, 8)
+    assert u["bad"] == 2 and u["n_union"] == 3
+    assert u["union_ids"][:3].tolist() == [0, 3, 5]
+
+
+# ---------------------------------------------------------------- chunk vs per-token
+
+def test_prefill_chunk_equals_per_token_bit_exact(oracle_mod):
+    W = synth.layer_weights(128, 16, 64, 4, seed=30, rms_norm=True)
+    L = oracle_layer(W)
+    r = bits(synth.hidden(9, 128, seed=31))
+    chunk = oracle_mod.prefill_chunk(L, r)
+    for t in range(9):
+        tok = oracle_mod.moe_token(L, r[t])
+        assert np.array_equal(chunk["idx"][t], tok["idx"])
+        assert np.array_equal(chunk["w"][t], tok["w"])
+        assert np.array_equal(chunk["y"][t], tok["y"])
+        assert np.array_equal(chunk["y_bf16"][t], tok["y_bf16"])
+    batch = oracle_mod.moe_tokens(L, r)
+    assert np.array_equal(batch["y"], chunk["y"])
+
+
+# ---------------------------------------------------------------- hand-worked fixture
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                key, *rest = line.split()
+                vals[key] = rest
+    return vals
+
+
+def test_hand_worked_layer(oracle_mod):
+    g = _read_golden("hand_worked_constant_experts.txt")
+    D, F, E, K = (int(g[k][0]) for k in ("D", "F", "E", "K"))
+    W = synth.layer_weights(D, E, F, K, seed=0)
+    v = [float(a) for a in g["router_v"]]
+    W.router_w = torch.tensor([[ve / 64] * D for ve in v]).to(torch.bfloat16)
+    for mat, key in (("gate", "const_gate"), ("up", "const_up"), ("down", "const_down")):
+        s = getattr(W, mat + "_s")
+        setattr(W, mat + "_s", torch.zeros_like(s))
+        c = torch.tensor([float(a) for a in g[key]]).view(E, 1, 1).expand_as(s)
+        setattr(W, mat + "_b", c.to(torch.bfloat16).contiguous())
+    out = oracle_mod.moe_token(oracle_layer(W), np.full(D, 0x3F80, np.uint16))
+    assert out["idx"].tolist() == [int(a) for a in g["expect_idx"]]
+    np.testing.assert_allclose(out["w"], [float(a) for a in g["expect_w"]], rtol=1e-15)
+    np.testing.assert_allclose(out["expert_out"][:, 0], [float(a) for a in g["expect_o"]],
+                               rtol=1e-14)
+    np.testing.assert_allclose(out["y"], float(g["expect_y"][0]), rtol=1e-15)
+    assert np.all(out["y_bf16"] == int(g["expect_y_bf16"][0], 16))

@@ -1,0 +1,52 @@
+"""Helpers shared by the tests: moving the seeded inputs between torch and the
+oracle's numpy view (bf16 as uint16 bits)."""
+import numpy as np
+import torch
+
+from oracle.oracle import OracleLayer
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 bit patterns (host numpy)."""
+    assert t.dtype == torch.bfloat16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def from_bits(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(
+        torch.bfloat16)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return bits(t)
+    return t.detach().cpu().contiguous().numpy()
+
+
+def oracle_layer(W) -> OracleLayer:
+    """synth.LayerWeights (any device) -> OracleLayer on the same bytes."""
+    return OracleLayer(
+        d_model=W.d_model, n_experts=W.n_experts, top_k=W.top_k, ffn_dim=W.ffn_dim,
+        router_w=host(W.router_w), gate_q=host(W.gate_q), gate_s=host(W.gate_s),
+        gate_b=host(W.gate_b), up_q=host(W.up_q), up_s=host(W.up_s), up_b=host(W.up_b),
+        down_q=host(W.down_q), down_s=host(W.down_s), down_b=host(W.down_b),
+        rms_gain=None if W.rms_gain is None else host(W.rms_gain), rms_eps=W.rms_eps,
+        norm_topk_prob=W.norm_topk_prob)
+
+
+def bf16_f64(a: np.ndarray) -> np.ndarray:
+    with np.errstate(invalid="ignore"):
+        return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+            np.float64)
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def max_row_rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64).reshape(np.shape(b)[0], -1)
+    b = np.asarray(b, np.float64).reshape(np.shape(b)[0], -1)
+    return max(rel_l2(a[i], b[i]) for i in range(b.shape[0]))
