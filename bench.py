@@ -1,0 +1,515 @@
+"""Benchmark of the routed-MoE hot path on one GB300 (or N replicas).
+
+Headline workload: a 30B-shaped 48-layer MoE decode stack at batch 1
+(d_model 2048, 128 experts, top-8, ffn 768, SMOE-Q4 group 64, RMSNorm before
+every router), 256 seeded N(0,1) start states.  One step = one decode token
+through all 48 layers (router + top-k + fused Q4 expert FFN + weighted
+residual sum, per layer), replayed from a CUDA graph; inputs are resident in
+HBM and each token reads 1.04 GB of distinct expert weights, more than L2.
+
+The JSON line also carries: the roofline of the dominant work (the decode
+expert FFN, timed per call with CUDA events), the end-to-end rate through the
+C ABI with host buffers, clocks sampled during the timed region, the oracle's
+CPU rate, a 235B-shaped 94-layer decode (per-token and per-layer time) and a
+235B-shaped layer-major prefill (prompts of 45, 512 and 4096 tokens in
+chunks of 64, tokens correlated so a chunk's union holds ~60-100 experts).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (the only other implementation of
+this path) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = ("MoE decode tokens/s (b=1) + expert-FFN effective HBM GB/s vs peak; prefill tok/s")
+D30, E, K, F30, L30 = 2048, 128, 8, 768, 48
+D235, F235, L235 = 4096, 1536, 94
+SEED = 1337
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def expert_bytes(D, F):
+    # codes + bf16 scale + bf16 bias for gate, up (F x D) and down (D x F)
+    per_matrix = D * F // 2 + 2 * 2 * (D * F // 64)
+    return 3 * per_matrix
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile(name, source_files):
+    """DRAM bytes per launch recorded in profiles/<name>.md, if the kernels it
+    was taken on are unchanged (sha256 of their sources matches)."""
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", txt)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256()
+    for f in source_files:
+        cur.update(open(os.path.join(ROOT, f), "rb").read())
+    if not cur.hexdigest().startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class DecodeStack:
+    """A stack of decode layers driven through the C ABI (one shared workspace)."""
+
+    def __init__(self, smoe, synth, n_layers, D, F, seed, dev):
+        self.smoe = smoe
+        self.W = [synth.layer_weights(D, E, F, K, seed=seed * 1000 + i, device=dev, rms_norm=True)
+                  for i in range(n_layers)]
+        self.L = [smoe.Layer(w) for w in self.W]
+        self.ws = smoe.workspace(self.L[0], 64)
+        self.D, self.F, self.n = D, F, n_layers
+        self.bufs = [torch.empty(D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+
+    def token(self, x_in, y_out):
+        """One token through all layers: x_in -> ... -> y_out (ping-pong in between)."""
+        cur = x_in
+        for i, L in enumerate(self.L):
+            nxt = y_out if i == self.n - 1 else self.bufs[i % 2]
+            self.smoe.smoe_moe_decode(L, cur, nxt, ws=self.ws)
+            cur = nxt
+
+
+def capture(fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm (module loads, attributes) outside the graph
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_decode(stack, states, steps, warmup, batch):
+    """Device-timed decode: graph of `batch` tokens (each from its own start
+    state) replayed until `steps` tokens ran; returns (ms per token, total ms)."""
+    D = stack.D
+    x_in = torch.empty((batch, D), dtype=torch.bfloat16, device=states.device)
+    y_out = torch.empty((batch, D), dtype=torch.bfloat16, device=states.device)
+
+    def run():
+        for t in range(batch):
+            stack.token(x_in[t], y_out[t])
+
+    g = capture(run)
+    n_states = states.shape[0]
+    reps = steps // batch
+    for r in range(max(1, (warmup + batch - 1) // batch)):
+        x_in.copy_(states[(r * batch) % n_states:(r * batch) % n_states + batch])
+        g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for r in range(reps):
+        base = (r * batch) % n_states
+        x_in.copy_(states[base:base + batch])
+        g.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    return ms / (reps * batch), ms
+
+
+def time_e2e(stack, states_host, steps, warmup):
+    """End to end: per token, H2D of its start state from pinned memory, the
+    48-layer decode, D2H of the output -- all inside the timed region."""
+    dev = stack.bufs[0].device
+    D = stack.D
+    x_dev = torch.empty(D, dtype=torch.bfloat16, device=dev)
+    y_dev = torch.empty(D, dtype=torch.bfloat16, device=dev)
+    y_host = torch.empty((steps, D), dtype=torch.bfloat16).pin_memory()
+    g = capture(lambda: stack.token(x_dev, y_dev))
+    n = states_host.shape[0]
+    for t in range(warmup):
+        x_dev.copy_(states_host[t % n], non_blocking=True)
+        g.replay()
+        y_host[t % steps].copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for t in range(steps):
+        x_dev.copy_(states_host[t % n], non_blocking=True)
+        g.replay()
+        y_host[t].copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return steps / dt, D * 2, D * 2
+
+
+def time_ffn(stack, states, n_tokens):
+    """Average duration of the expert FFN call (gate/up + down/combine kernels)
+    per layer, CUDA events on the launching stream, over n_tokens x layers."""
+    smoe = stack.smoe
+    dev = states.device
+    idx = torch.empty(K, dtype=torch.int32, device=dev)
+    w = torch.empty(K, dtype=torch.float32, device=dev)
+    evs = []
+    stream = torch.cuda.current_stream()
+    for t in range(n_tokens):
+        cur = states[t % states.shape[0]].clone()
+        nxt = torch.empty_like(cur)
+        for L in stack.L:
+            smoe.smoe_route_topk(L, cur, 1, idx, w, ws=stack.ws)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            smoe.smoe_moe_ffn_decode(L, cur, idx, w, nxt, ws=stack.ws)
+            b.record(stream)
+            evs.append((a, b))
+            cur, nxt = nxt, cur
+    torch.cuda.synchronize()
+    durs = [a.elapsed_time(b) for a, b in evs]
+    return sum(durs) / len(durs)
+
+
+def calibrate_alpha(smoe, synth, L0, dev, lo=0.0, hi=0.95, target=(60, 100)):
+    """Shared-direction weight alpha so that a 64-token chunk's layer-0 union
+    lands in [60, 100] experts (bisection on the GPU router)."""
+    idx = torch.empty((64, K), dtype=torch.int32, device=dev)
+    w = torch.empty((64, K), dtype=torch.float32, device=dev)
+    ws = smoe.workspace(L0, 64)
+    u = 0
+    for _ in range(20):
+        a = 0.5 * (lo + hi)
+        x = synth.correlated_hidden(64, L0.w.d_model, a, seed=SEED, device=dev)
+        smoe.smoe_route_topk(L0, x, 64, idx, w, ws=ws)
+        u = int(torch.unique(idx).numel())
+        if target[0] <= u <= target[1]:
+            return a, u
+        if u > target[1]:
+            lo = a
+        else:
+            hi = a
+    return a, u
+
+
+def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
+    """Layer-major prefill over the 235B stack: each 64-token chunk goes
+    through all layers (per layer: route, union, grouped FFN, combine)."""
+    res = {}
+    T = 64
+    ws = stack.ws
+    xa = torch.empty((T, stack.D), dtype=torch.bfloat16, device=dev)
+    bufs = [torch.empty((T, stack.D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+
+    def chunk(t):
+        cur = xa[:t]
+        for i, L in enumerate(stack.L):
+            nxt = bufs[i % 2][:t]
+            smoe.smoe_moe_prefill_chunk(L, cur, t, nxt, idx_out=idx[:t] if i == 0 else None, ws=ws)
+            cur = nxt
+
+    graphs = {T: capture(lambda: chunk(T))}
+    unions = []
+    for n in prompt_lens:
+        x = synth.correlated_hidden(n, stack.D, alpha, seed=SEED + n, device=dev)
+        tail = n % T
+        if tail and tail not in graphs:
+            graphs[tail] = capture(lambda: chunk(tail))
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for c0 in range(0, n, T):
+            t = min(T, n - c0)
+            xa[:t].copy_(x[c0:c0 + t])
+            graphs[t].replay()
+        ev1.record()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        # union size of the last chunk's first layer
+        unions.append(int(torch.unique(idx[:min(T, n - (n - 1) // T * T)]).numel()))
+        res[str(n)] = {"ms": round(ms, 3), "tok_s": round(n / ms * 1e3, 1),
+                       "chunks": (n + T - 1) // T}
+    return res, unions
+
+
+def cpu_baseline_oracle(stack, states, n_tokens, n_layers):
+    """The oracle (as it stands) on n_tokens decode tokens through the first
+    n_layers of the same stack, tokens in parallel on the host cores; the rate
+    is scaled to the full stack depth."""
+    import numpy as np
+    from oracle import oracle
+    from tests.util import oracle_layer
+    oracle.build()
+    OL = [oracle_layer(w) for w in stack.W[:n_layers]]
+    x = states[:n_tokens].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    cur = x
+    for L in OL:
+        out = oracle.moe_tokens(L, cur)
+        cur = out["y_bf16"]
+    dt = time.perf_counter() - t0
+    per_token_full = dt / n_tokens * (stack.n / n_layers)
+    return {"value": round(1.0 / per_token_full, 4), "unit": "tok/s", "cores": oracle.omp_threads(),
+            "kind": "oracle",
+            "sample": f"{n_tokens} tokens x first {n_layers} of {stack.n} layers "
+                      f"({dt:.1f} s wall), rate scaled to {stack.n} layers"}
+
+
+def our_arm(args):
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", local if ws_ > 1 else 0)
+    torch.cuda.set_device(dev)
+    from quantised_expert_ffn_gb300 import build
+    build.build()
+    from quantised_expert_ffn_gb300 import smoe, synth
+
+    hbm_peak, peak_kind = peaks()
+    log(f"[bench] building 30B stack ({L30} layers)")
+    stack = DecodeStack(smoe, synth, L30, D30, F30, SEED, dev)
+    states = synth.hidden(256, D30, seed=SEED, device=dev)
+    batch = 16 if args.steps % 16 == 0 else (8 if args.steps % 8 == 0 else 1)
+
+    # ---- headline: device-timed decode, clocks sampled during the timed region
+    time_decode(stack, states, batch, batch, batch)   # compile graph paths once
+    with Clocks(dev.index) as ck:
+        ms_tok, ms_total = time_decode(stack, states, args.steps, args.warmup, batch)
+    clocks = ck.summary()
+    if ws_ > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+        ms_tok = ms_total / args.steps
+    value = args.steps * ws_ / (ms_total / 1e3)
+    bytes_token = L30 * (K * expert_bytes(D30, F30) + E * D30 * 2)
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": ws_,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_tok, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded random SMOE-Q4 weights and N(0,1) start states)",
+            "config": {"workload": "30B-shaped 48-layer MoE decode stack, batch 1 (d_model 2048, "
+                                   "128 experts, top-8, ffn 768, SMOE-Q4 group 64, RMSNorm)",
+                       "layers": L30, "global_batch": 1, "start_states": 256,
+                       "l2": "inputs larger than L2: each token reads "
+                             f"{bytes_token / 1e9:.2f} GB of distinct weights",
+                       "parallelism": "replicas" if ws_ > 1 else "single GPU",
+                       "graph_tokens": batch},
+            "effective_gbs_per_token": round(bytes_token / (ms_tok / 1e3) / 1e9, 1),
+            "clocks": clocks,
+            "gpu_launches": args.steps * L30 * 3}
+
+    if rank == 0:
+        # ---- roofline of the dominant work: the decode expert FFN call
+        ffn_ms = time_ffn(stack, states, 8)
+        ffn_bytes = K * expert_bytes(D30, F30)
+        achieved = ffn_bytes / (ffn_ms / 1e3) / 1e9
+        traffic = traffic_from_profile(
+            "decode_ffn_30b", ["quantised_expert_ffn_gb300/csrc/decode.cu",
+                               "quantised_expert_ffn_gb300/csrc/common.cuh"])
+        line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                            "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                            "traffic": traffic, "peak_kind": peak_kind,
+                            "kernel": "decode expert FFN (gate/up + down/combine), 8 experts",
+                            "bytes_per_launch": ffn_bytes, "ms_per_launch": round(ffn_ms, 5)}
+        # ---- end to end through the C ABI with host buffers
+        states_host = states[:64].cpu().pin_memory()
+        e2e, bi, bo = time_e2e(stack, states_host, args.steps, max(3, args.warmup))
+        line["e2e"] = {"value": round(e2e, 2), "unit": "tok/s", "h2d_bytes_per_step": bi,
+                       "d2h_bytes_per_step": bo}
+        if ws_ == 1 and not args.no_cpu:
+            log("[bench] timing the oracle on the host cores")
+            line["cpu_baseline"] = cpu_baseline_oracle(stack, states, args.cpu_tokens,
+                                                       args.cpu_layers)
+    del stack
+    torch.cuda.empty_cache()
+
+    if rank == 0 and ws_ == 1 and not args.no_235b:
+        log(f"[bench] building 235B stack ({L235} layers, ~128 GB)")
+        big = DecodeStack(smoe, synth, L235, D235, F235, SEED + 1, dev)
+        st235 = synth.hidden(128, D235, seed=SEED + 1, device=dev)
+        ms235, _ = time_decode(big, st235, 128, 16, 16)
+        b235 = L235 * (K * expert_bytes(D235, F235) + E * D235 * 2)
+        line["decode_235b"] = {"workload": "235B-shaped 94-layer MoE decode, batch 1 (d_model "
+                                           "4096, ffn 1536), 128 tokens",
+                               "tok_s": round(1e3 / ms235, 2), "ms_per_token": round(ms235, 4),
+                               "us_per_layer": round(ms235 * 1e3 / L235, 2),
+                               "effective_gbs": round(b235 / (ms235 / 1e3) / 1e9, 1)}
+        alpha, u0 = calibrate_alpha(smoe, synth, big.L[0], dev)
+        pre, unions = time_prefill(big, smoe, synth, dev, [45, 512, 4096], alpha)
+        line["prefill"] = {"workload": "235B-shaped 94-layer layer-major prefill, chunks of 64",
+                           "alpha": round(alpha, 4), "layer0_union_64tok": u0, "prompts": pre,
+                           "tok_s_4096": pre["4096"]["tok_s"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def reference_arm(args):
+    """The CPU oracle timed as it stands, on a bounded sample of the headline
+    workload (30B-shaped 48-layer decode, same seeded weights)."""
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    from oracle import oracle
+    from quantised_expert_ffn_gb300 import synth
+    from tests.util import oracle_layer
+    oracle.build()
+    n_layers = args.cpu_layers
+    W = [synth.layer_weights(D30, E, F30, K, seed=SEED * 1000 + i, device="cpu", rms_norm=True)
+         for i in range(n_layers)]
+    OL = [oracle_layer(w) for w in W]
+    states = synth.hidden(256, D30, seed=SEED, device="cpu")
+    x_all = states.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ntok = args.cpu_tokens
+
+    def step(i):
+        cur = x_all[(i * ntok) % 256:(i * ntok) % 256 + ntok]
+        for L in OL:
+            cur = oracle.moe_tokens(L, cur)["y_bf16"]
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    per_token_full = dt / (args.steps * ntok) * (L30 / n_layers)
+    value = 1.0 / per_token_full
+    sample = (f"{ntok} tokens x first {n_layers} of {L30} layers per step, rate scaled to "
+              f"{L30} layers")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tok/s",
+            "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_token_full * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded random SMOE-Q4 weights and N(0,1) start states)",
+            "config": {"workload": "30B-shaped 48-layer MoE decode stack, batch 1 (d_model 2048, "
+                                   "128 experts, top-8, ffn 768, SMOE-Q4 group 64, RMSNorm)",
+                       "layers": L30, "global_batch": 1},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tok/s",
+                             "cores": oracle.omp_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=16)
+    ap.add_argument("--cpu-layers", type=int, default=4)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-235b", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if args.steps > 4 and "--steps" not in " ".join(sys.argv):
+            args.steps = 2
+        reference_arm(args)
+    else:
+        our_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * smoe.h -- C ABI of libsmoe.so: the routed Mixture-of-Experts layer of the
+ * S-MoE engine (exact router gate -> top-k with norm_topk_prob weights ->
+ * per-chunk expert union and buckets -> SMOE-Q4 fused dequant expert FFN ->
+ * weighted sum into the residual), as CUDA kernels for sm_103a (GB300).
+ *
+ * Sources of the operations (the S-MoE documentation pages "Optimizations"
+ * and "System Overview"):
+ *   - exact routing on the true hidden state, top-8, norm_topk_prob mixing
+ *     weights: "Optimizations", section "Routing Is Exact -- Prompt and
+ *     Generation Alike"; "System Overview", table "What Happens at Each
+ *     Generated Token Step" (Heavy pass row);
+ *   - per-chunk expert union, chunks of up to 64 tokens: "Optimizations",
+ *     section "Prefill Reads Each Expert Once, Not Once Per Token";
+ *   - SMOE-Q4 fused dequant FFN, gate+up in one pass, weighted sum into the
+ *     residual: "Optimizations", section "Coalesced GPU Kernels -- Expert FFN
+ *     and Dense Matvec"; "System Overview", same table, Metal Kernel row;
+ *   - RMSNorm before the router (between layers): "Optimizations", section
+ *     "The Dense Ceiling -- GPU-Resident Epilogue";
+ *   - no allocation in the token loop: "Optimizations", section "Zero
+ *     Allocations, Zero Locks in the Token Loop".
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions shared by every entry point
+ *
+ * Memory.  Every pointer is caller-owned DEVICE memory unless a parameter
+ * says otherwise.  The library never allocates, never frees and never
+ * synchronises the stream; all work is enqueued on `stream` (the CUDA stream
+ * of the caller, cudaStream_t; NULL = legacy default stream), so every call
+ * can be captured into a CUDA graph.
+ *
+ * Types.  bf16 tensors are passed as smoe_bf16 (the raw 16-bit pattern of a
+ * bfloat16).  Shapes are row-major, outermost first.
+ *
+ * SMOE-Q4 weights (this layout is fixed here; the pages leave it open).  A
+ * matrix of `rows` outputs and `cols` inputs stores
+ *   codes  uint8 [rows][cols/2]: element 2j is the low nibble of byte j,
+ *          element 2j+1 the high nibble; code q in 0..15;
+ *   scale  bf16  [rows][cols/64]  and  bias bf16 [rows][cols/64];
+ *   weight w[r][c] = scale[r][c/64] * q[r][c] + bias[r][c/64].
+ * Within a layer the experts are contiguous: gate and up are [E][F][D]
+ * (codes [E][F][D/2], scale/bias [E][F][D/64]); down is [E][D][F]
+ * (codes [E][D][F/2], scale/bias [E][D][F/64]); the router is bf16 [E][D].
+ *
+ * Workspace.  Calls that need scratch take `ws`/`ws_bytes`: device memory of
+ * at least smoe_workspace_bytes() bytes, 256-byte aligned, that the caller
+ * zero-fills once before its first use (smoe_workspace_init() does it on the
+ * stream).  Each call leaves its counters zero again.  The first 4 bytes are
+ * the int32 DEVICE STATUS WORD: 0, or a negative smoe_status that a kernel
+ * found (an expert id out of range, a bounded wait that gave up).  Kernels
+ * only ever write a non-zero value there; the caller reads it after a
+ * synchronisation (smoe_read_device_status) and clears it with
+ * smoe_workspace_init().  Calls that share one workspace must not overlap on
+ * the GPU (the same stream, or ordered by events).
+ *
+ * Errors.  Problems the host can see (NULL pointers, unsupported shapes,
+ * misaligned pointers, a workspace that is too small) return a negative
+ * smoe_status at once and enqueue nothing.  A failed launch returns
+ * SMOE_ERR_CUDA.  Nothing throws across this ABI and no kernel traps.
+ *
+ * Supported shapes: d_model and ffn_dim multiples of 64 (group_size must be
+ * 64), d_model <= 8192, ffn_dim <= 4096, 1 <= top_k <= 16, top_k <= n_experts
+ * <= 256, top_k * ffn_dim <= 16384.  Code pointers and the hidden-state
+ * pointers must be 16-byte aligned.  Tuned for d_model 2048/4096, 128
+ * experts, top-8, ffn_dim 768/1536.
+ */
+#ifndef SMOE_H
+#define SMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t smoe_bf16;                /* raw bfloat16 bits */
+typedef struct CUstream_st *smoe_stream;   /* identical to cudaStream_t */
+
+typedef enum smoe_status {
+    SMOE_OK = 0,
+    SMOE_ERR_INVALID_ARG = -1,   /* NULL pointer, bad size or alignment */
+    SMOE_ERR_UNSUPPORTED = -2,   /* shape outside the supported set */
+    SMOE_ERR_WORKSPACE = -3,     /* workspace missing, misaligned or too small */
+    SMOE_ERR_CUDA = -4,          /* a CUDA launch or runtime call failed */
+    SMOE_ERR_TIMEOUT = -5,       /* device: a bounded wait gave up */
+    SMOE_ERR_DEVICE = -6         /* device: bad data (e.g. expert id out of range) */
+} smoe_status;
+
+/* One MoE layer: its shape and its device-resident parameters. */
+typedef struct smoe_layer {
+    int d_model;                 /* D: hidden size */
+    int n_experts;               /* E: routed experts */
+    int top_k;                   /* k: experts per token */
+    int ffn_dim;                 /* F: expert intermediate size */
+    int group_size;              /* Q4 group along the input dim; must be 64 */
+    int norm_topk_prob;          /* 1: renormalise the top-k probabilities to sum 1 */
+    float rms_eps;               /* RMSNorm epsilon (used when rms_gain != NULL) */
+    const smoe_bf16 *rms_gain;   /* [D] RMSNorm gain before the router and the FFN; NULL = none */
+    const smoe_bf16 *router_w;   /* [E][D] router gate */
+    const uint8_t *gate_q;       /* [E][F][D/2] */
+    const smoe_bf16 *gate_s;     /* [E][F][D/64] */
+    const smoe_bf16 *gate_b;     /* [E][F][D/64] */
+    const uint8_t *up_q;         /* [E][F][D/2] */
+    const smoe_bf16 *up_s;       /* [E][F][D/64] */
+    const smoe_bf16 *up_b;       /* [E][F][D/64] */
+    const uint8_t *down_q;       /* [E][D][F/2] */
+    const smoe_bf16 *down_s;     /* [E][D][F/64] */
+    const smoe_bf16 *down_b;     /* [E][D][F/64] */
+} smoe_layer;
+
+/* Bytes of workspace that the calls below need for this layer shape and up
+ * to `max_tokens` tokens per call (1 for decode, up to 64 for a prefill
+ * chunk).  Host only; returns 0 when the shape is unsupported. */
+size_t smoe_workspace_bytes(const smoe_layer *layer, int max_tokens);
+
+/* Zero `ws_bytes` bytes of workspace on `stream` (cudaMemsetAsync). */
+int smoe_workspace_init(void *ws, size_t ws_bytes, smoe_stream stream);
+
+/* Copy the device status word of `ws` to *status_host.  This one call
+ * synchronises `stream`.  Returns SMOE_OK or SMOE_ERR_CUDA. */
+int smoe_read_device_status(const void *ws, int32_t *status_host, smoe_stream stream);
+
+/* Router gate and top-k ("Routing Is Exact"; per-token table, Heavy pass).
+ * For each of T tokens x[t] (bf16 [T][D]):
+ *   xn = rms_gain ? bf16(x / sqrt(mean(x^2) + eps) * rms_gain) : x
+ *   logits[e] = sum_d router_w[e][d] * xn[d]           (fp32 accumulation)
+ *   idx[t][0..k)  = the k largest logits, descending; equal logits keep the
+ *                   lower expert id
+ *   w[t][i] = softmax(logits)[idx_i], renormalised over the k selected when
+ *             norm_topk_prob (then equal to a softmax over the k logits)
+ * Outputs: idx int32 [T][k], w fp32 [T][k]; logits_opt fp32 [T][E] and
+ * xn_opt bf16 [T][D] when non-NULL.  1 <= T <= 64. */
+int smoe_route_topk(const smoe_layer *layer, const smoe_bf16 *x, int T, int32_t *idx,
+                    float *w, float *logits_opt, smoe_bf16 *xn_opt, void *ws,
+                    size_t ws_bytes, smoe_stream stream);
+
+/* Per-chunk expert union and per-expert token buckets ("Prefill Reads Each
+ * Expert Once, Not Once Per Token").  idx int32 [T][k], w fp32 [T][k],
+ * 1 <= T <= 64, k <= 16, E <= 256.  Outputs (device):
+ *   union_ids  int32 [E]: the distinct ids of idx in ascending order, then -1;
+ *   n_union    int32 [1]: how many;
+ *   offsets    int32 [E+1]: bucket u is [offsets[u], offsets[u+1]); entries
+ *              past n_union hold the number of bucketed entries;
+ *   bucket_tok, bucket_rank int32 [T*k], bucket_w fp32 [T*k]: for each union
+ *              expert in order, its tokens ascending (a token that lists the
+ *              expert twice appears once per listing, in rank order), with the
+ *              rank i at which the token chose it and w[t][i]; unused tail
+ *              entries are -1 / -1 / 0.
+ * Ids outside [0, E) are skipped and set *status_dev (device int32, may be
+ * NULL) to SMOE_ERR_DEVICE. */
+int smoe_expert_union(const int32_t *idx, const float *w, int T, int k, int E,
+                      int32_t *union_ids, int32_t *n_union, int32_t *offsets,
+                      int32_t *bucket_tok, int32_t *bucket_rank, float *bucket_w,
+                      int32_t *status_dev, smoe_stream stream);
+
+/* One decode token through the layer (batch 1):
+ *   route x as smoe_route_topk; for each selected expert i (rank order)
+ *   h = SiLU(Wgate_e xn) * (Wup_e xn)  [F],   o_i = Wdown_e h  [D]
+ *   y = x + sum_i w_i o_i   (fp32, one rounding to bf16)
+ * x, y bf16 [D] (y may alias x).  Optional outputs: idx_out int32 [k],
+ * w_out fp32 [k], expert_out fp32 [k][D] (the unweighted o_i). */
+int smoe_moe_decode(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
+                    int32_t *idx_out_opt, float *w_out_opt, float *expert_out_opt, void *ws,
+                    size_t ws_bytes, smoe_stream stream);
+
+/* The expert FFN of one decode token for a routing already made (the Metal
+ * Kernel row of the per-token table: the SMOE-Q4 fused FFN of each claimed
+ * expert, weighted-summed into the residual):
+ *   xn = RMSNorm(x) as in smoe_route_topk;  for i in 0..k-1, e = idx[i]:
+ *   o_i = Wdown_e (SiLU(Wgate_e xn) * (Wup_e xn));  y = x + sum_i w[i] o_i.
+ * idx int32 [k] and w fp32 [k] are device arrays (e.g. smoe_route_topk's
+ * outputs); an id outside [0, E) contributes nothing and sets the device
+ * status word.  x, y bf16 [D] (y may alias x); expert_out fp32 [k][D] or NULL.
+ * smoe_moe_decode is smoe_route_topk followed by this call. */
+int smoe_moe_ffn_decode(const smoe_layer *layer, const smoe_bf16 *x, const int32_t *idx,
+                        const float *w, smoe_bf16 *y, float *expert_out_opt, void *ws,
+                        size_t ws_bytes, smoe_stream stream);
+
+/* One prefill chunk of T tokens (1 <= T <= 64) through the layer: route all
+ * tokens, build the expert union and buckets on the device, read each union
+ * expert's weights once and apply them to every token of its bucket (grouped
+ * GEMM on the tensor cores), then y[t] = x[t] + sum_i w[t][i] o[t][i] in rank
+ * order.  x, y bf16 [T][D] (y must not alias x).  Optional outputs:
+ * idx_out int32 [T][k], w_out fp32 [T][k]. */
+int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
+                           int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
+                           smoe_stream stream);
+
+/* A static string naming a status code. */
+const char *smoe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMOE_H */

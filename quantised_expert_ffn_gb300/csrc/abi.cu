@@ -1,0 +1,280 @@
+// abi.cu -- the extern "C" entry points of libsmoe.so (declared in include/smoe.h):
+// host-side argument checks, workspace layout and kernel launches.  No entry
+// point allocates, frees or synchronises (smoe_read_device_status excepted,
+// which exists to synchronise).
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smoe {
+
+cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float *h32,
+                                cudaStream_t s, bool pdl);
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Byte offsets of the workspace sections for a layer shape and a token count.
+struct WsLayout {
+    size_t status, counters, idx, w, logits, xn, xn16, h, n_union, union_ids, offsets,
+        bucket_tok, bucket_rank, bucket_w, slot_of, h32, hbuf, xperm, obuf, total;
+};
+
+WsLayout ws_layout(const smoe_layer &L, int T) {
+    WsLayout o{};
+    const size_t D = L.d_model, E = L.n_experts, K = L.top_k, F = L.ffn_dim;
+    const size_t TK = (size_t)T * K;
+    size_t p = 0;
+    o.status = p;      p += kAlign;                       // int32 status word (+ padding)
+    o.counters = p;    p = up(p + kMaxChunk * 4);
+    o.idx = p;         p = up(p + TK * 4);
+    o.w = p;           p = up(p + TK * 4);
+    o.logits = p;      p = up(p + (size_t)T * E * 4);
+    o.xn = p;          p = up(p + (size_t)T * D * 2);
+    o.xn16 = p;        p = up(p + (size_t)T * D * 2);
+    o.h = p;           p = up(p + K * F * 4);
+    o.n_union = p;     p = up(p + 4);
+    o.union_ids = p;   p = up(p + E * 4);
+    o.offsets = p;     p = up(p + (E + 1) * 4);
+    o.bucket_tok = p;  p = up(p + TK * 4);
+    o.bucket_rank = p; p = up(p + TK * 4);
+    o.bucket_w = p;    p = up(p + TK * 4);
+    o.slot_of = p;     p = up(p + TK * 4);
+    o.h32 = p;         p = up(p + TK * F * 4);
+    o.hbuf = p;        p = up(p + TK * F * 2);
+    o.xperm = p;       p = up(p + TK * D * 2);
+    o.obuf = p;        p = up(p + TK * D * 4);
+    o.total = p;
+    return o;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_layer(const smoe_layer *L) {
+    if (!L) return SMOE_ERR_INVALID_ARG;
+    if (!L->router_w || !L->gate_q || !L->gate_s || !L->gate_b || !L->up_q || !L->up_s ||
+        !L->up_b || !L->down_q || !L->down_s || !L->down_b)
+        return SMOE_ERR_INVALID_ARG;
+    if (L->group_size != kGroup) return SMOE_ERR_UNSUPPORTED;
+    const int D = L->d_model, E = L->n_experts, K = L->top_k, F = L->ffn_dim;
+    if (D <= 0 || F <= 0 || E <= 0 || K <= 0) return SMOE_ERR_INVALID_ARG;
+    if (D % kGroup || F % kGroup) return SMOE_ERR_UNSUPPORTED;
+    if (D > kMaxD || F > kMaxF || E > kMaxExperts || K > kMaxTopK || K > E || K * F > kMaxKF)
+        return SMOE_ERR_UNSUPPORTED;
+    if (!aligned(L->router_w, 16) || !aligned(L->gate_q, 16) || !aligned(L->up_q, 16) ||
+        !aligned(L->down_q, 16))
+        return SMOE_ERR_INVALID_ARG;
+    if (!aligned(L->gate_s, 2) || !aligned(L->gate_b, 2) || !aligned(L->up_s, 2) ||
+        !aligned(L->up_b, 2) || !aligned(L->down_s, 2) || !aligned(L->down_b, 2) ||
+        (L->rms_gain && !aligned(L->rms_gain, 2)))
+        return SMOE_ERR_INVALID_ARG;
+    if (L->rms_gain && !(L->rms_eps >= 0.f)) return SMOE_ERR_INVALID_ARG;
+    return SMOE_OK;
+}
+
+int check_ws(const smoe_layer *L, int T, void *ws, size_t ws_bytes) {
+    if (!ws || !aligned(ws, kAlign)) return SMOE_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*L, T).total) return SMOE_ERR_WORKSPACE;
+    return SMOE_OK;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA; }
+
+RouteArgs route_args(const smoe_layer &L, const smoe_bf16 *x, void *ws, const WsLayout &o,
+                     int32_t *idx, float *w, float *logits, smoe_bf16 *xn, __half *xn16) {
+    RouteArgs r{};
+    r.x = x;
+    r.gain = L.rms_gain;
+    r.eps = L.rms_eps;
+    r.router_w = L.router_w;
+    r.D = L.d_model;
+    r.E = L.n_experts;
+    r.K = L.top_k;
+    r.norm_topk_prob = L.norm_topk_prob ? 1 : 0;
+    r.logits = logits ? logits : at<float>(ws, o.logits);
+    r.idx = idx;
+    r.w = w;
+    r.xn_out = xn;
+    r.xn16_out = xn16;
+    r.counters = at<int32_t>(ws, o.counters);
+    return r;
+}
+
+}  // namespace
+}  // namespace smoe
+
+using namespace smoe;
+
+extern "C" {
+
+size_t smoe_workspace_bytes(const smoe_layer *layer, int max_tokens) {
+    if (check_layer(layer) != SMOE_OK || max_tokens < 1 || max_tokens > kMaxChunk) return 0;
+    return ws_layout(*layer, max_tokens).total;
+}
+
+int smoe_workspace_init(void *ws, size_t ws_bytes, smoe_stream stream) {
+    if (!ws || ws_bytes == 0) return SMOE_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+int smoe_read_device_status(const void *ws, int32_t *status_host, smoe_stream stream) {
+    if (!ws || !status_host) return SMOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(status_host, ws, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+int smoe_route_topk(const smoe_layer *layer, const smoe_bf16 *x, int T, int32_t *idx, float *w,
+                    float *logits_opt, smoe_bf16 *xn_opt, void *ws, size_t ws_bytes,
+                    smoe_stream stream) {
+    int st = check_layer(layer);
+    if (st != SMOE_OK) return st;
+    if (!x || !idx || !w || T < 1 || T > kMaxChunk) return SMOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (xn_opt && !aligned(xn_opt, 2))) return SMOE_ERR_INVALID_ARG;
+    if ((st = check_ws(layer, T, ws, ws_bytes)) != SMOE_OK) return st;
+    const WsLayout o = ws_layout(*layer, T);
+    RouteArgs r = route_args(*layer, x, ws, o, idx, w, logits_opt, xn_opt, nullptr);
+    return cuda_status(launch_route_topk(r, T, (cudaStream_t)stream, true));
+}
+
+int smoe_expert_union(const int32_t *idx, const float *w, int T, int k, int E, int32_t *union_ids,
+                      int32_t *n_union, int32_t *offsets, int32_t *bucket_tok,
+                      int32_t *bucket_rank, float *bucket_w, int32_t *status_dev,
+                      smoe_stream stream) {
+    if (!idx || !w || !union_ids || !n_union || !offsets || !bucket_tok || !bucket_rank ||
+        !bucket_w)
+        return SMOE_ERR_INVALID_ARG;
+    if (T < 1 || T > kMaxChunk || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts)
+        return SMOE_ERR_INVALID_ARG;
+    UnionArgs u{idx, w, T, k, E, union_ids, n_union, offsets, bucket_tok, bucket_rank,
+                bucket_w, status_dev, nullptr};
+    return cuda_status(launch_expert_union(u, (cudaStream_t)stream, true));
+}
+
+static int launch_ffn_decode(const smoe_layer &L, const smoe_bf16 *x, const int32_t *idx,
+                             const float *w, smoe_bf16 *y, float *expert_out, void *ws,
+                             const WsLayout &o, cudaStream_t s) {
+    DecodeArgs d{};
+    d.x = x;
+    d.gain = L.rms_gain;
+    d.eps = L.rms_eps;
+    d.D = L.d_model;
+    d.F = L.ffn_dim;
+    d.K = L.top_k;
+    d.E = L.n_experts;
+    d.idx = idx;
+    d.w = w;
+    d.gq = L.gate_q; d.gs = L.gate_s; d.gb = L.gate_b;
+    d.uq = L.up_q;   d.us = L.up_s;   d.ub = L.up_b;
+    d.dq = L.down_q; d.ds = L.down_s; d.db = L.down_b;
+    d.h = at<float>(ws, o.h);
+    d.y = y;
+    d.expert_out = expert_out;
+    d.status = at<int32_t>(ws, o.status);
+    if (launch_decode_gateup(d, s, true) != cudaSuccess) return SMOE_ERR_CUDA;
+    return cuda_status(launch_decode_down(d, s, true));
+}
+
+int smoe_moe_ffn_decode(const smoe_layer *layer, const smoe_bf16 *x, const int32_t *idx,
+                        const float *w, smoe_bf16 *y, float *expert_out_opt, void *ws,
+                        size_t ws_bytes, smoe_stream stream) {
+    int st = check_layer(layer);
+    if (st != SMOE_OK) return st;
+    if (!x || !y || !idx || !w || !aligned(x, 16) || !aligned(y, 16)) return SMOE_ERR_INVALID_ARG;
+    if (expert_out_opt && !aligned(expert_out_opt, 4)) return SMOE_ERR_INVALID_ARG;
+    if ((st = check_ws(layer, 1, ws, ws_bytes)) != SMOE_OK) return st;
+    return launch_ffn_decode(*layer, x, idx, w, y, expert_out_opt, ws, ws_layout(*layer, 1),
+                             (cudaStream_t)stream);
+}
+
+int smoe_moe_decode(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
+                    int32_t *idx_out_opt, float *w_out_opt, float *expert_out_opt, void *ws,
+                    size_t ws_bytes, smoe_stream stream) {
+    int st = check_layer(layer);
+    if (st != SMOE_OK) return st;
+    if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return SMOE_ERR_INVALID_ARG;
+    if (expert_out_opt && !aligned(expert_out_opt, 4)) return SMOE_ERR_INVALID_ARG;
+    if ((st = check_ws(layer, 1, ws, ws_bytes)) != SMOE_OK) return st;
+    const WsLayout o = ws_layout(*layer, 1);
+    int32_t *idx = idx_out_opt ? idx_out_opt : at<int32_t>(ws, o.idx);
+    float *w = w_out_opt ? w_out_opt : at<float>(ws, o.w);
+    cudaStream_t s = (cudaStream_t)stream;
+    RouteArgs r = route_args(*layer, x, ws, o, idx, w, nullptr, nullptr, nullptr);
+    if (launch_route_topk(r, 1, s, true) != cudaSuccess) return SMOE_ERR_CUDA;
+    return launch_ffn_decode(*layer, x, idx, w, y, expert_out_opt, ws, o, s);
+}
+
+int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
+                           int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
+                           smoe_stream stream) {
+    int st = check_layer(layer);
+    if (st != SMOE_OK) return st;
+    if (!x || !y || T < 1 || T > kMaxChunk || !aligned(x, 16) || !aligned(y, 16) || x == y)
+        return SMOE_ERR_INVALID_ARG;
+    if ((st = check_ws(layer, T, ws, ws_bytes)) != SMOE_OK) return st;
+    const smoe_layer &L = *layer;
+    const WsLayout o = ws_layout(L, T);
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t *idx = idx_out_opt ? idx_out_opt : at<int32_t>(ws, o.idx);
+    float *w = w_out_opt ? w_out_opt : at<float>(ws, o.w);
+    RouteArgs r = route_args(L, x, ws, o, idx, w, nullptr, at<smoe_bf16>(ws, o.xn),
+                             at<__half>(ws, o.xn16));
+    cudaError_t e = launch_route_topk(r, T, s, true);
+    if (e != cudaSuccess) return SMOE_ERR_CUDA;
+    UnionArgs u{idx, w, T, L.top_k, L.n_experts, at<int32_t>(ws, o.union_ids),
+                at<int32_t>(ws, o.n_union), at<int32_t>(ws, o.offsets),
+                at<int32_t>(ws, o.bucket_tok), at<int32_t>(ws, o.bucket_rank),
+                at<float>(ws, o.bucket_w), at<int32_t>(ws, o.status), at<int32_t>(ws, o.slot_of)};
+    if ((e = launch_expert_union(u, s, true)) != cudaSuccess) return SMOE_ERR_CUDA;
+    PrefillArgs p{};
+    p.x = x;
+    p.T = T;
+    p.D = L.d_model;
+    p.F = L.ffn_dim;
+    p.K = L.top_k;
+    p.E = L.n_experts;
+    p.xn16 = at<__half>(ws, o.xn16);
+    p.n_union = u.n_union;
+    p.union_ids = u.union_ids;
+    p.offsets = u.offsets;
+    p.bucket_tok = u.bucket_tok;
+    p.bucket_rank = u.bucket_rank;
+    p.slot_of = u.slot_of;
+    p.w = w;
+    p.gq = L.gate_q; p.gs = L.gate_s; p.gb = L.gate_b;
+    p.uq = L.up_q;   p.us = L.up_s;   p.ub = L.up_b;
+    p.dq = L.down_q; p.ds = L.down_s; p.db = L.down_b;
+    p.xperm = at<__half>(ws, o.xperm);
+    p.hbuf = at<__half>(ws, o.hbuf);
+    p.obuf = at<float>(ws, o.obuf);
+    p.y = y;
+    p.status = at<int32_t>(ws, o.status);
+    p.num_sms = device_sm_count();
+    return cuda_status(launch_prefill_simt(p, at<smoe_bf16>(ws, o.xn), at<float>(ws, o.h32), s, true));
+}
+
+const char *smoe_status_string(int status) {
+    switch (status) {
+    case SMOE_OK: return "SMOE_OK";
+    case SMOE_ERR_INVALID_ARG: return "SMOE_ERR_INVALID_ARG: NULL pointer, bad size or alignment";
+    case SMOE_ERR_UNSUPPORTED: return "SMOE_ERR_UNSUPPORTED: shape outside the supported set";
+    case SMOE_ERR_WORKSPACE: return "SMOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case SMOE_ERR_CUDA: return "SMOE_ERR_CUDA: a CUDA launch or runtime call failed";
+    case SMOE_ERR_TIMEOUT: return "SMOE_ERR_TIMEOUT: a bounded device wait gave up";
+    case SMOE_ERR_DEVICE: return "SMOE_ERR_DEVICE: bad data found on the device";
+    default: return "unknown smoe status";
+    }
+}
+
+}  // extern "C"

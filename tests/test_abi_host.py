@@ -1,0 +1,110 @@
+"""Host-only checks of the C ABI (no GPU needed): the library loads, exports
+every entry point that include/smoe.h declares, and rejects bad arguments on
+the host before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantised_expert_ffn_gb300 import build
+    build.build()
+    from quantised_expert_ffn_gb300 import smoe
+    return smoe
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(smoe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_prefill_chunk",
+              "smoe_workspace_bytes", "smoe_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(so, n), n
+    assert set(declared_functions()) <= set(lib.EXPORTED) | {"smoe_status_string"}
+
+
+def _layer(lib, D=2048, E=128, K=8, F=768, ptr=1 << 20):
+    s = lib.smoe_layer()
+    s.d_model, s.n_experts, s.top_k, s.ffn_dim, s.group_size, s.norm_topk_prob = D, E, K, F, 64, 1
+    s.rms_eps = 1e-6
+    for n in ("router_w", "gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q",
+              "down_s", "down_b"):
+        setattr(s, n, ptr)
+    return s
+
+
+def test_workspace_bytes_and_shape_checks(lib):
+    so = lib._lib
+    s = _layer(lib)
+    n1 = so.smoe_workspace_bytes(ctypes.byref(s), 1)
+    n64 = so.smoe_workspace_bytes(ctypes.byref(s), 64)
+    assert 0 < n1 < n64 and n64 % 256 == 0
+    assert so.smoe_workspace_bytes(ctypes.byref(s), 65) == 0
+    assert so.smoe_workspace_bytes(ctypes.byref(s), 0) == 0
+    for bad in (dict(D=2000), dict(F=700), dict(K=0), dict(K=17), dict(E=300), dict(E=4, K=8),
+                dict(D=16384), dict(F=4096, K=8)):
+        assert so.smoe_workspace_bytes(ctypes.byref(_layer(lib, **bad)), 1) == 0, bad
+    g = _layer(lib)
+    g.group_size = 32
+    assert so.smoe_workspace_bytes(ctypes.byref(g), 1) == 0
+    assert so.smoe_workspace_bytes(None, 1) == 0
+
+
+def test_entry_points_reject_bad_arguments_on_host(lib):
+    so = lib._lib
+    s = _layer(lib)
+    ref = ctypes.byref(s)
+    ws = ctypes.c_void_p(1 << 24)
+    n = so.smoe_workspace_bytes(ref, 64)
+    P = ctypes.c_void_p
+    # NULL layer / NULL tensors
+    assert so.smoe_moe_decode(None, P(4096), P(8192), None, None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_moe_decode(ref, None, P(8192), None, None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    # misaligned hidden state
+    assert so.smoe_moe_decode(ref, P(4098), P(8192), None, None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    # workspace too small / missing / misaligned
+    assert so.smoe_moe_decode(ref, P(4096), P(8192), None, None, None, ws, 16, None) == lib.SMOE_ERR_WORKSPACE
+    assert so.smoe_moe_decode(ref, P(4096), P(8192), None, None, None, None, n, None) == lib.SMOE_ERR_WORKSPACE
+    assert so.smoe_moe_decode(ref, P(4096), P(8192), None, None, None, P((1 << 24) + 8), n, None) == lib.SMOE_ERR_WORKSPACE
+    # prefill: T out of range, aliasing
+    assert so.smoe_moe_prefill_chunk(ref, P(4096), 0, P(8192), None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_moe_prefill_chunk(ref, P(4096), 65, P(8192), None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_moe_prefill_chunk(ref, P(4096), 4, P(4096), None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    # route: T range, NULL outputs
+    assert so.smoe_route_topk(ref, P(4096), 65, P(64), P(128), None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_route_topk(ref, P(4096), 1, None, P(128), None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    # union: sizes
+    args = [P(64)] * 2
+    outs = [P(256)] * 6
+    assert so.smoe_expert_union(*args, 65, 8, 128, *outs, None, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_expert_union(*args, 4, 17, 128, *outs, None, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_expert_union(*args, 4, 8, 257, *outs, None, None) == lib.SMOE_ERR_INVALID_ARG
+    # unsupported layer shape
+    bad = _layer(lib, D=2000)
+    assert so.smoe_moe_decode(ctypes.byref(bad), P(4096), P(8192), None, None, None, ws, n, None) == lib.SMOE_ERR_UNSUPPORTED
+    # misaligned codes
+    mis = _layer(lib)
+    mis.gate_q = (1 << 20) + 4
+    assert so.smoe_moe_decode(ctypes.byref(mis), P(4096), P(8192), None, None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        assert lib.smoe_status_string(code).startswith("SMOE_")
+    assert "unknown" in lib.smoe_status_string(7)

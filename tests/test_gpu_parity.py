@@ -1,0 +1,283 @@
+"""GPU parity: every entry point of libsmoe.so, called through the C ABI,
+against the CPU oracle on the same seeded bytes.
+
+Bars: top-k ids, union lists and buckets bit-exact; mixing weights 1e-6
+relative (given the same logits); FFN outputs and the residual output within
+2e-3 relative L2 per token.  Inputs are drawn with routing margins (see
+tests.util.margin_tokens) so that fp32 and fp64 logits rank alike."""
+import numpy as np
+import pytest
+import torch
+
+from quantised_expert_ffn_gb300 import synth
+from tests.util import (bf16_f64, bits, from_bits, host, margin_tokens, max_row_rel_l2,
+                        oracle_layer, rel_l2)
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def smoe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantised_expert_ffn_gb300 import build
+    build.build()
+    from quantised_expert_ffn_gb300 import smoe as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    from oracle import oracle
+    oracle.build()
+    return oracle
+
+
+SHAPES = {
+    "tiny": (128, 16, 4, 128),
+    "odd": (192, 24, 3, 320),        # D/64 = 3 groups, F/32 = 10 chunks: ragged lanes
+    "30b": (2048, 128, 8, 768),
+    "235b": (4096, 128, 8, 1536),
+}
+_cache = {}
+
+
+def layer(name, norm, seed=1337, ntp=True):
+    key = (name, norm, seed, ntp)
+    if key not in _cache:
+        D, E, K, F = SHAPES[name]
+        W = synth.layer_weights(D, E, F, K, seed=seed, device="cuda", rms_norm=norm,
+                                norm_topk_prob=ntp)
+        _cache.clear()
+        _cache[key] = (W, oracle_layer(W))
+    return _cache[key]
+
+
+def dev(a):
+    if a.dtype == np.uint16:
+        return from_bits(a).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# ------------------------------------------------------------------------- route
+
+@pytest.mark.parametrize("name,norm,T", [("tiny", False, 1), ("tiny", True, 64), ("odd", True, 5),
+                                         ("30b", False, 1), ("30b", True, 45), ("235b", True, 64)])
+def test_route_topk(smoe, orc, name, norm, T):
+    W, OL = layer(name, norm)
+    D, E, K = W.d_model, W.n_experts, W.top_k
+    x = margin_tokens(OL, T, seed=T)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, T)
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    xn = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    smoe.smoe_route_topk(L, dev(x), T, idx, w, logits, xn, ws)
+    torch.cuda.synchronize()
+    assert smoe.smoe_read_device_status(ws) == 0
+    idx, w, logits, xn = host(idx), host(w), host(logits), host(xn)
+    for t in range(T):
+        o = orc.moe_token(OL, x[t]) if T <= 8 else None
+        xn_ref = orc.rmsnorm(OL, x[t])
+        diff = xn[t] != xn_ref
+        # fp32 vs fp64 normalisation may round a rare element the other way
+        assert diff.sum() <= max(2, D // 500)
+        assert np.all(np.abs(xn[t][diff].astype(np.int32) - xn_ref[diff].astype(np.int32)) == 1)
+        lg_ref = orc.router_logits(OL, xn[t])             # same normed input as the GPU used
+        scale = np.abs(bf16_f64(OL.router_w)) @ np.abs(bf16_f64(xn[t]))
+        assert np.all(np.abs(logits[t] - lg_ref) <= 1e-6 * scale + 1e-30)
+        idx_ref = orc.topk(orc.router_logits(OL, xn_ref), K)
+        assert np.array_equal(idx[t], idx_ref), (t, idx[t], idx_ref)
+        w_same_logits = orc.mix_weights(logits[t].astype(np.float64), idx[t], True)
+        np.testing.assert_allclose(w[t], w_same_logits, rtol=1e-6, atol=0)
+        if o is not None:
+            np.testing.assert_allclose(w[t], o["w"], rtol=2e-5)
+
+
+def test_route_without_norm_topk_prob(smoe, orc):
+    W, OL = layer("tiny", True, ntp=False)
+    x = margin_tokens(OL, 3, seed=5)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 3)
+    idx = torch.empty((3, 4), dtype=torch.int32, device="cuda")
+    w = torch.empty((3, 4), dtype=torch.float32, device="cuda")
+    logits = torch.empty((3, 16), dtype=torch.float32, device="cuda")
+    smoe.smoe_route_topk(L, dev(x), 3, idx, w, logits, None, ws)
+    torch.cuda.synchronize()
+    for t in range(3):
+        lg = host(logits)[t].astype(np.float64)
+        ref = orc.mix_weights(lg, host(idx)[t], False)
+        np.testing.assert_allclose(host(w)[t], ref, rtol=1e-6)
+        assert host(w)[t].sum() < 1.0
+
+
+# ------------------------------------------------------------------------- union
+
+def _union_gpu(smoe, idx_np, w_np, E):
+    T, k = idx_np.shape
+    d = lambda n, dt=torch.int32: torch.full((n,), -7, dtype=dt, device="cuda")
+    out = dict(union_ids=d(E), n_union=d(1), offsets=d(E + 1), bucket_tok=d(T * k),
+               bucket_rank=d(T * k), bucket_w=torch.full((T * k,), -7.0, device="cuda"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    smoe.smoe_expert_union(dev(idx_np.astype(np.int32)), dev(w_np.astype(np.float32)), T, k, E,
+                           out["union_ids"], out["n_union"], out["offsets"], out["bucket_tok"],
+                           out["bucket_rank"], out["bucket_w"], status)
+    torch.cuda.synchronize()
+    return {k_: host(v) for k_, v in out.items()}, int(host(status)[0])
+
+
+def _zipf_idx(rng, T, k, E, s=1.2):
+    p = np.arange(1, E + 1, dtype=np.float64) ** -s
+    p = p[rng.permutation(E)]
+    p /= p.sum()
+    return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)])
+
+
+@pytest.mark.parametrize("T,k,E,kind", [(1, 8, 128, "rand"), (45, 8, 128, "rand"),
+                                        (64, 8, 128, "rand"), (64, 8, 128, "zipf"),
+                                        (64, 8, 128, "same"), (16, 8, 128, "distinct"),
+                                        (64, 16, 256, "rand"), (13, 3, 5, "rand")])
+def test_expert_union(smoe, orc, T, k, E, kind):
+    rng = np.random.default_rng(T * 131 + k + E)
+    if kind == "rand":
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    elif kind == "zipf":
+        idx = _zipf_idx(rng, T, k, E)
+    elif kind == "same":
+        idx = np.tile(rng.permutation(E)[:k], (T, 1))
+    else:
+        idx = np.arange(T * k).reshape(T, k) % E
+    w = rng.random((T, k)).astype(np.float32)
+    got, status = _union_gpu(smoe, idx, w, E)
+    ref = orc.expert_union(idx, E)
+    assert status == 0
+    assert int(got["n_union"][0]) == ref["n_union"]
+    for key in ("union_ids", "offsets", "bucket_tok", "bucket_rank"):
+        assert np.array_equal(got[key], ref[key]), key
+    n = ref["offsets"][ref["n_union"]]
+    assert np.array_equal(got["bucket_w"][:n], w[ref["bucket_tok"][:n], ref["bucket_rank"][:n]])
+    assert np.all(got["bucket_w"][n:] == 0)
+    if kind == "same":
+        assert ref["n_union"] == k
+    if kind == "distinct":
+        assert ref["n_union"] == min(E, T * k)
+
+
+def test_expert_union_bad_ids_set_status(smoe, orc):
+    idx = np.array([[0, 5, 200], [-1, 5, 3]])
+    got, status = _union_gpu(smoe, idx, np.ones((2, 3)), 8)
+    ref = orc.expert_union(idx, 8)
+    assert status == smoe.SMOE_ERR_DEVICE
+    assert int(got["n_union"][0]) == ref["n_union"] == 3
+    for key in ("union_ids", "offsets", "bucket_tok", "bucket_rank"):
+        assert np.array_equal(got[key], ref[key]), key
+
+
+# ------------------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("name,norm,ntok", [("tiny", False, 6), ("odd", True, 4), ("30b", False, 6),
+                                            ("30b", True, 6), ("235b", True, 3)])
+def test_moe_decode(smoe, orc, name, norm, ntok):
+    W, OL = layer(name, norm)
+    D, K = W.d_model, W.top_k
+    x = margin_tokens(OL, ntok, seed=100 + ntok)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 1)
+    for t in range(ntok):
+        xt = dev(x[t])
+        y = torch.empty_like(xt)
+        idx = torch.empty(K, dtype=torch.int32, device="cuda")
+        w = torch.empty(K, dtype=torch.float32, device="cuda")
+        eo = torch.empty((K, D), dtype=torch.float32, device="cuda")
+        smoe.smoe_moe_decode(L, xt, y, idx, w, eo, ws)
+        torch.cuda.synchronize()
+        ref = orc.moe_token(OL, x[t])
+        assert np.array_equal(host(idx), ref["idx"])
+        np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
+        assert max_row_rel_l2(host(eo), ref["expert_out"]) <= TOL
+        assert rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+    assert smoe.smoe_read_device_status(ws) == 0
+
+
+def test_moe_decode_in_place(smoe, orc):
+    W, OL = layer("30b", True)
+    x = margin_tokens(OL, 1, seed=3)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 1)
+    xt = dev(x[0])
+    y_sep = torch.empty_like(xt)
+    smoe.smoe_moe_decode(L, xt, y_sep, ws=ws)
+    smoe.smoe_moe_decode(L, xt, xt, ws=ws)           # y aliases x
+    torch.cuda.synchronize()
+    assert torch.equal(xt, y_sep)
+
+
+def test_decode_workspace_left_clean(smoe):
+    W, _ = layer("tiny", True)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 1)
+    x = synth.hidden(1, W.d_model, seed=2, device="cuda")[0]
+    for _ in range(5):
+        smoe.smoe_moe_decode(L, x, torch.empty_like(x), ws=ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(ws[:512]).item() == 0    # status word and route tickets
+
+
+# ------------------------------------------------------------------------- prefill
+
+@pytest.mark.parametrize("name,norm,T,alpha", [("tiny", False, 1, None), ("tiny", True, 64, None),
+                                               ("odd", True, 13, None), ("30b", True, 45, None),
+                                               ("30b", True, 64, 0.7), ("235b", True, 64, 0.6),
+                                               ("235b", False, 7, None)])
+def test_moe_prefill_chunk(smoe, orc, name, norm, T, alpha):
+    W, OL = layer(name, norm)
+    K = W.top_k
+    x = margin_tokens(OL, T, seed=200 + T, alpha=alpha)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, T)
+    y = torch.empty((T, W.d_model), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, dev(x), T, y, idx, w, ws)
+    torch.cuda.synchronize()
+    assert smoe.smoe_read_device_status(ws) == 0
+    ref = orc.moe_tokens(OL, x)                    # = the chunk path, bit for bit (oracle pin)
+    assert np.array_equal(host(idx), ref["idx"])
+    np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
+    assert max_row_rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+
+
+def test_prefill_matches_decode_on_gpu(smoe, orc):
+    W, OL = layer("30b", True)
+    T = 16
+    x = dev(margin_tokens(OL, T, seed=77))
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, T)
+    yc = torch.empty_like(x)
+    idc = torch.empty((T, 8), dtype=torch.int32, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, x, T, yc, idc, None, ws)
+    for t in range(T):
+        yd = torch.empty_like(x[t])
+        idd = torch.empty(8, dtype=torch.int32, device="cuda")
+        smoe.smoe_moe_decode(L, x[t], yd, idd, None, None, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(idd, idc[t])
+        assert rel_l2(yd.float().cpu().numpy(), yc[t].float().cpu().numpy()) <= TOL
+
+
+def test_prefill_all_tokens_one_bucket(smoe, orc):
+    """Every token identical: the union is exactly k experts, each bucket holds all T tokens."""
+    W, OL = layer("30b", True)
+    x1 = margin_tokens(OL, 1, seed=9)
+    x = np.repeat(x1, 64, axis=0)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 64)
+    y = torch.empty((64, W.d_model), dtype=torch.bfloat16, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, dev(x), 64, y, ws=ws)
+    torch.cuda.synchronize()
+    ref = orc.moe_token(OL, x1[0])
+    yh = bf16_f64(host(y))
+    assert rel_l2(yh[0], ref["y"]) <= TOL
+    assert np.all(yh == yh[0])

@@ -50,3 +50,31 @@ def max_row_rel_l2(a, b) -> float:
     a = np.asarray(a, np.float64).reshape(np.shape(b)[0], -1)
     b = np.asarray(b, np.float64).reshape(np.shape(b)[0], -1)
     return max(rel_l2(a[i], b[i]) for i in range(b.shape[0]))
+
+
+def margin_tokens(OL, n, seed, *, alpha=None, tau_factor=10.0, max_tries=50):
+    """n hidden states (bf16 [n, D], host) whose oracle routing has every
+    adjacent gap among ranks 1..k+1 at least tau_factor * tau, with
+    tau = 64 * 2^-24 * max_e sum_d |Wr[e][d] xn[d]| (so the GPU's fp32 logits
+    rank the same experts in the same order).  Candidates come from the seeded
+    generator (independent, or sharing a direction when alpha is given)."""
+    from oracle import oracle
+    from quantised_expert_ffn_gb300 import synth
+    D, k = OL.d_model, OL.top_k
+    Wabs = np.abs(bf16_f64(OL.router_w))
+    keep = []
+    for attempt in range(max_tries):
+        if alpha is None:
+            cand = bits(synth.hidden(2 * n, D, seed=seed * 7919 + attempt))
+        else:
+            cand = bits(synth.correlated_hidden(2 * n, D, alpha, seed=seed * 7919 + attempt))
+        for r in cand:
+            xn = oracle.rmsnorm(OL, r)
+            lg = oracle.router_logits(OL, xn)
+            tau = 64 * 2.0 ** -24 * float((Wabs @ np.abs(bf16_f64(xn))).max())
+            top = np.sort(lg)[::-1][:k + 1]
+            if top.size < 2 or np.all(top[:-1] - top[1:] >= tau_factor * tau):
+                keep.append(r)
+                if len(keep) == n:
+                    return np.stack(keep)
+    raise RuntimeError("could not draw enough tokens with routing margins")
