@@ -297,7 +297,6 @@ def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
             cur = nxt
 
     graphs = {T: capture(lambda: chunk(T))}
-    unions = []
     for n in prompt_lens:
         x = synth.correlated_hidden(n, stack.D, alpha, seed=SEED + n, device=dev)
         tail = n % T
@@ -313,11 +312,9 @@ def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
         ev1.record()
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1)
-        # union size of the last chunk's first layer
-        unions.append(int(torch.unique(idx[:min(T, n - (n - 1) // T * T)]).numel()))
         res[str(n)] = {"ms": round(ms, 3), "tok_s": round(n / ms * 1e3, 1),
                        "chunks": (n + T - 1) // T}
-    return res, unions
+    return res
 
 
 def cpu_baseline_oracle(stack, states, n_tokens, n_layers):
@@ -341,6 +338,29 @@ def cpu_baseline_oracle(stack, states, n_tokens, n_layers):
             "kind": "oracle",
             "sample": f"{n_tokens} tokens x first {n_layers} of {stack.n} layers "
                       f"({dt:.1f} s wall), rate scaled to {stack.n} layers"}
+
+
+def profile_case(args):
+    """Small case for ncu captures: an N-layer 30B-shaped stack (a few GB),
+    a few decode tokens and one 64-token prefill chunk through each layer,
+    launched directly (no graph).  Prints no JSON line."""
+    dev = torch.device("cuda", 0)
+    from quantised_expert_ffn_gb300 import build
+    build.build()
+    from quantised_expert_ffn_gb300 import smoe, synth
+    n = args.profile_layers
+    shape = (D235, F235) if args.profile_shape == "235b" else (D30, F30)
+    stack = DecodeStack(smoe, synth, n, shape[0], shape[1], SEED, dev)
+    states = synth.hidden(8, shape[0], seed=SEED, device=dev)
+    y = torch.empty(shape[0], dtype=torch.bfloat16, device=dev)
+    for t in range(4):
+        stack.token(states[t], y)
+    x64 = synth.correlated_hidden(64, shape[0], 0.6, seed=SEED, device=dev)
+    y64 = torch.empty_like(x64)
+    for L in stack.L:
+        smoe.smoe_moe_prefill_chunk(L, x64, 64, y64, ws=stack.ws)
+    torch.cuda.synchronize()
+    log(f"[bench] profile case done: {n} layers of {shape}")
 
 
 def our_arm(args):
@@ -427,7 +447,7 @@ def our_arm(args):
                                "us_per_layer": round(ms235 * 1e3 / L235, 2),
                                "effective_gbs": round(b235 / (ms235 / 1e3) / 1e9, 1)}
         alpha, u0 = calibrate_alpha(smoe, synth, big.L[0], dev)
-        pre, unions = time_prefill(big, smoe, synth, dev, [45, 512, 4096], alpha)
+        pre = time_prefill(big, smoe, synth, dev, [45, 512, 4096], alpha)
         line["prefill"] = {"workload": "235B-shaped 94-layer layer-major prefill, chunks of 64",
                            "alpha": round(alpha, 4), "layer0_union_64tok": u0, "prompts": pre,
                            "tok_s_4096": pre["4096"]["tok_s"]}
@@ -500,7 +520,13 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=4)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-235b", action="store_true")
+    ap.add_argument("--profile-layers", type=int, default=0,
+                    help="run only the small ncu case with this many layers")
+    ap.add_argument("--profile-shape", default="30b", choices=["30b", "235b"])
     args = ap.parse_args()
+    if args.profile_layers:
+        profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -3,15 +3,13 @@
 // point allocates, frees or synchronises (smoe_read_device_status excepted,
 // which exists to synchronise).
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
 
 namespace smoe {
-
-cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float *h32,
-                                cudaStream_t s, bool pdl);
 
 namespace {
 
@@ -21,7 +19,7 @@ size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Byte offsets of the workspace sections for a layer shape and a token count.
 struct WsLayout {
-    size_t status, counters, idx, w, logits, xn, xn16, h, n_union, union_ids, offsets,
+    size_t status, counters, gbar, idx, w, logits, xn, xn16, h, n_union, union_ids, offsets,
         bucket_tok, bucket_rank, bucket_w, slot_of, h32, hbuf, xperm, obuf, total;
 };
 
@@ -32,6 +30,7 @@ WsLayout ws_layout(const smoe_layer &L, int T) {
     size_t p = 0;
     o.status = p;      p += kAlign;                       // int32 status word (+ padding)
     o.counters = p;    p = up(p + kMaxChunk * 4);
+    o.gbar = p;        p = up(p + 8);                    // grid barrier {count, generation}
     o.idx = p;         p = up(p + TK * 4);
     o.w = p;           p = up(p + TK * 4);
     o.logits = p;      p = up(p + (size_t)T * E * 4);
@@ -89,6 +88,29 @@ T *at(void *ws, size_t off) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA; }
+
+// Decode engine: 1 = fused one-kernel layer, 0 = three kernels (router, gate/up,
+// down).  SMOE_DECODE_PATH=split selects the latter (cross-check).
+int decode_path() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("SMOE_DECODE_PATH");
+        v = (e && strcmp(e, "split") == 0) ? 0 : 1;
+    }
+    return v;
+}
+
+// Prefill FFN engine: 1 = tensor cores (tcgen05), 0 = CUDA cores.  Both are
+// hand-written kernels of this library; SMOE_PREFILL_PATH=simt selects the
+// CUDA-core one (used to cross-check the two).
+int prefill_path() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("SMOE_PREFILL_PATH");
+        v = (e && strcmp(e, "simt") == 0) ? 0 : 1;
+    }
+    return v;
+}
 
 RouteArgs route_args(const smoe_layer &L, const smoe_bf16 *x, void *ws, const WsLayout &o,
                      int32_t *idx, float *w, float *logits, smoe_bf16 *xn, __half *xn16) {
@@ -162,9 +184,42 @@ int smoe_expert_union(const int32_t *idx, const float *w, int T, int k, int E, i
     return cuda_status(launch_expert_union(u, (cudaStream_t)stream, true));
 }
 
-static int launch_ffn_decode(const smoe_layer &L, const smoe_bf16 *x, const int32_t *idx,
-                             const float *w, smoe_bf16 *y, float *expert_out, void *ws,
-                             const WsLayout &o, cudaStream_t s) {
+// Decode FFN (and routing when idx_in is NULL): the fused one-kernel layer
+// when the shape fits its plan, else the three-kernel path.
+static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int32_t *idx_in,
+                              const float *w_in, int32_t *idx_out, float *w_out, smoe_bf16 *y,
+                              float *expert_out, void *ws, const WsLayout &o, cudaStream_t s) {
+    FusedArgs f{};
+    f.x = x;
+    f.y = y;
+    f.gain = L.rms_gain;
+    f.eps = L.rms_eps;
+    f.D = L.d_model;
+    f.F = L.ffn_dim;
+    f.K = L.top_k;
+    f.E = L.n_experts;
+    f.norm_topk_prob = L.norm_topk_prob ? 1 : 0;
+    f.router_w = L.router_w;
+    f.gq = L.gate_q; f.gs = L.gate_s; f.gb = L.gate_b;
+    f.uq = L.up_q;   f.us = L.up_s;   f.ub = L.up_b;
+    f.dq = L.down_q; f.ds = L.down_s; f.db = L.down_b;
+    f.logits = at<float>(ws, o.logits);
+    f.h = at<float>(ws, o.h);
+    f.bar = at<uint32_t>(ws, o.gbar);
+    f.status = at<int32_t>(ws, o.status);
+    f.idx_out = idx_out;
+    f.w_out = w_out;
+    f.idx_in = idx_in;
+    f.w_in = w_in;
+    f.expert_out = expert_out;
+    if (decode_path() == 1 && fused_plan(f, device_sm_count()))
+        return cuda_status(launch_decode_layer(f, s, idx_in == nullptr));
+    if (!idx_in) {
+        RouteArgs r = route_args(L, x, ws, o, idx_out, w_out, nullptr, nullptr, nullptr);
+        if (launch_route_topk(r, 1, s, true) != cudaSuccess) return SMOE_ERR_CUDA;
+        idx_in = idx_out;
+        w_in = w_out;
+    }
     DecodeArgs d{};
     d.x = x;
     d.gain = L.rms_gain;
@@ -173,8 +228,8 @@ static int launch_ffn_decode(const smoe_layer &L, const smoe_bf16 *x, const int3
     d.F = L.ffn_dim;
     d.K = L.top_k;
     d.E = L.n_experts;
-    d.idx = idx;
-    d.w = w;
+    d.idx = idx_in;
+    d.w = w_in;
     d.gq = L.gate_q; d.gs = L.gate_s; d.gb = L.gate_b;
     d.uq = L.up_q;   d.us = L.up_s;   d.ub = L.up_b;
     d.dq = L.down_q; d.ds = L.down_s; d.db = L.down_b;
@@ -194,8 +249,8 @@ int smoe_moe_ffn_decode(const smoe_layer *layer, const smoe_bf16 *x, const int32
     if (!x || !y || !idx || !w || !aligned(x, 16) || !aligned(y, 16)) return SMOE_ERR_INVALID_ARG;
     if (expert_out_opt && !aligned(expert_out_opt, 4)) return SMOE_ERR_INVALID_ARG;
     if ((st = check_ws(layer, 1, ws, ws_bytes)) != SMOE_OK) return st;
-    return launch_ffn_decode(*layer, x, idx, w, y, expert_out_opt, ws, ws_layout(*layer, 1),
-                             (cudaStream_t)stream);
+    return launch_decode_path(*layer, x, idx, w, nullptr, nullptr, y, expert_out_opt, ws,
+                              ws_layout(*layer, 1), (cudaStream_t)stream);
 }
 
 int smoe_moe_decode(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
@@ -209,10 +264,8 @@ int smoe_moe_decode(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
     const WsLayout o = ws_layout(*layer, 1);
     int32_t *idx = idx_out_opt ? idx_out_opt : at<int32_t>(ws, o.idx);
     float *w = w_out_opt ? w_out_opt : at<float>(ws, o.w);
-    cudaStream_t s = (cudaStream_t)stream;
-    RouteArgs r = route_args(*layer, x, ws, o, idx, w, nullptr, nullptr, nullptr);
-    if (launch_route_topk(r, 1, s, true) != cudaSuccess) return SMOE_ERR_CUDA;
-    return launch_ffn_decode(*layer, x, idx, w, y, expert_out_opt, ws, o, s);
+    return launch_decode_path(*layer, x, nullptr, nullptr, idx, w, y, expert_out_opt, ws, o,
+                              (cudaStream_t)stream);
 }
 
 int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
@@ -261,6 +314,10 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     p.y = y;
     p.status = at<int32_t>(ws, o.status);
     p.num_sms = device_sm_count();
+    if (prefill_path() == 1 && prefill_tc_supported(p.D, p.F)) {
+        if (launch_prefill_tc(p, s) != cudaSuccess) return SMOE_ERR_CUDA;
+        return cuda_status(launch_prefill_combine(p, s, true));
+    }
     return cuda_status(launch_prefill_simt(p, at<smoe_bf16>(ws, o.xn), at<float>(ws, o.h32), s, true));
 }
 

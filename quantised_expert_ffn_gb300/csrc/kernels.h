@@ -76,6 +76,31 @@ struct DecodeArgs {
 cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t s, bool pdl);
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t s, bool pdl);
 
+// One decode layer as one persistent kernel (decode_fused.cu).
+struct FusedArgs {
+    const uint16_t *x;          // [D] residual in
+    uint16_t *y;                // [D] out (may alias x)
+    const uint16_t *gain;       // RMSNorm gain or NULL
+    float eps;
+    int D, F, K, E, norm_topk_prob;
+    const uint16_t *router_w;
+    const uint8_t *gq, *uq, *dq;
+    const uint16_t *gs, *gb, *us, *ub, *ds, *db;
+    float *logits;              // [E] scratch
+    float *h;                   // [K][F] scratch
+    uint32_t *bar;              // grid barrier {count, generation}
+    int32_t *status;
+    int32_t *idx_out;           // [K] (route variant)
+    float *w_out;               // [K]
+    const int32_t *idx_in;      // [K] (FFN-only variant)
+    const float *w_in;          // [K]
+    float *expert_out;          // [K][D] or NULL
+    // plan (fused_plan)
+    int grid, r_gu, e_dn, dn_gran, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
+};
+bool fused_plan(FusedArgs &a, int num_sms);
+cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route);
+
 struct PrefillArgs {
     const uint16_t *x;          // [T][D] residual
     int T, D, F, K, E;
@@ -96,7 +121,13 @@ struct PrefillArgs {
     int32_t *status;
     int num_sms;
 };
-cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s, bool pdl);
+// CUDA-core path: gate/up, down and combine (fp32 h)
+cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float *h32, cudaStream_t s,
+                                bool pdl);
+// tensor-core path: bucket gather, gate/up and down grouped GEMMs (fp16 h); combine separately
+bool prefill_tc_supported(int D, int F);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_combine(const PrefillArgs &a, cudaStream_t s, bool pdl);
 
 int device_sm_count();
 

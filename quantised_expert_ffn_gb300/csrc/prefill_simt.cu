@@ -162,6 +162,10 @@ __global__ void __launch_bounds__(kThreads) k_prefill_combine(PrefillArgs a) {
     }
 }
 
+cudaError_t launch_prefill_combine(const PrefillArgs &a, cudaStream_t s, bool pdl) {
+    return launch_kernel(k_prefill_combine, dim3(a.T), dim3(kThreads), 0, s, pdl, a);
+}
+
 cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float *h32,
                                 cudaStream_t s, bool pdl) {
     SimtArgs sa{a, xn, h32};

@@ -1,0 +1,572 @@
+// prefill_tc.cu -- prefill chunk FFN as grouped per-expert GEMMs on the
+// 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA staging).
+//
+// "Optimizations" page, "Prefill Reads Each Expert Once, Not Once Per Token":
+// a chunk's routed experts are deduplicated into a union that is read once;
+// here each union expert's Q4 rows are streamed from HBM once and multiplied
+// with all the tokens of its bucket.  The pages' token-batch prefill FFN
+// kernels keep a thread-per-row layout ("The Dense Ceiling" section); on GB300
+// the bucket makes the work a real (if skinny) contraction, so it runs on the
+// tensor cores with the weights as the 128-row M side ("swap AB") and the
+// bucket's tokens as N (padded to a multiple of 16, at most 64).
+//
+// One persistent CTA per SM walks a static list of units (union expert u,
+// 128-row tile); per unit the K dimension is consumed in chunks of 64 (one Q4
+// group, one 128-byte swizzle atom).  Warp roles:
+//   warps 0-7   dequant: read the TMA-staged codes of a chunk from shared
+//               memory, turn them into fp16 w = s*q + b (one rounding; exact
+//               when b = -8 s, since s*(q-8) needs at most 11 bits) and
+//               write the A tile in the 128-byte-swizzled K-major layout;
+//   warp 12     TMA: codes tiles (no swizzle) and the bucket's activation
+//               tile (128-byte swizzle) into a ring of stages;
+//   warp 13     MMA: one thread issues tcgen05.mma (M=128, N=pad16(bucket),
+//               K=16, fp16 x fp16 -> fp32 in TMEM) and commits stages back;
+//   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
+//               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
+//               (gate/up kernel) or the fp32 expert outputs (down kernel).
+// Two TMEM accumulator buffers let the epilogue of one unit overlap the main
+// loop of the next.  Every wait on an mbarrier is bounded: on timeout the CTA
+// records SMOE_ERR_TIMEOUT, all roles drain and the TMEM is freed.
+//
+// The dequant writes the 8 elements of each 32-bit code word as the pairs
+// (e0,e4),(e1,e5),(e2,e6),(e3,e7) -- the order the fp16 magic-number unpack
+// produces them in.  The activation side (x for gate/up, h for down) is stored
+// with the same permutation of each 8-element block, so the contraction is
+// unchanged.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smoe {
+
+namespace {
+
+constexpr int kTcThreads = 448;
+constexpr int kProdThreads = 256;    // warps 0-7
+constexpr int kEpiWarp0 = 8;         // warps 8-11
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kTile = 128;
+constexpr int kKc = 64;
+constexpr int kNmax = 64;
+constexpr int kStages = 6;
+constexpr int kAStages = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;
+constexpr uint32_t kUpCol = 128;
+constexpr int kCodeBytes = kTile * kKc / 2;          // 4 KB of codes per matrix per stage
+constexpr int kATileBytes = kTile * kKc * 2;         // 16 KB fp16 A tile
+constexpr int kBTileBytes = kNmax * kKc * 2;         // 8 KB fp16 B tile (up to 64 rows)
+constexpr long long kSpinLimit = 1ll << 22;
+
+struct TcParams {
+    int n_tiles;            // 128-row tiles per expert
+    int n_chunks;           // K / 64
+    int rows_per_expert;    // F (gate/up) or D (down)
+    int k_dim;              // K (D or F)
+    int out_ld;             // row length of the output (F for h, D for o)
+    const int32_t *n_union, *union_ids, *offsets;
+    const uint16_t *s0, *b0, *s1, *b1;   // scales/biases of A0 (gate or down) and A1 (up)
+    __half *hout;           // gate/up: h [slots][F] fp16, K-permuted
+    float *oout;            // down: o [slots][D] fp32
+    int32_t *status;
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(b))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
+                     smem_u32(b)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
+    for (long long i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try(b, parity)) return true;
+        if ((i & 1023) == 1023 && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    set_status(status, SMOE_ERR_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// K-major operand in the 128-byte swizzle: rows of 128 bytes, 8-row groups
+// 1024 bytes apart (stride byte offset), leading byte offset unused.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+    d |= (uint64_t)1 << 46;                 // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp16 A and B (K-major), fp32 D, M x N.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.u32 p, %4, 0;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+        " [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- dequant ---------------------------------------------------------------
+
+// 8 codes of one word -> 4 half2 (e_i, e_{i+4}), each s*q + b with one rounding.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
+    const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t m;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(m) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x64006400u));
+        __half2 q = __hsub2(*reinterpret_cast<__half2 *>(&m), k1024);   // exact q
+        __half2 v = __hfma2(q, s2, b2);                                   // s*q + b, one rounding
+        o[i] = *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+__device__ __forceinline__ int perm8(int f) {   // position of element f in the permuted order
+    const int i = f & 7;
+    return (f & ~7) | (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+}
+
+template <bool kPair>
+struct Smem {
+    static constexpr int kMats = kPair ? 2 : 1;
+    static constexpr int kStageBytes = kMats * kCodeBytes + kBTileBytes;
+    static constexpr int kAOff = 0;
+    static constexpr int kStageOff = kAStages * kMats * kATileBytes;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kBytes = kBarOff + 1024;   // barriers + tmem slot + flags
+};
+
+template <bool kPair>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_prefill_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                 const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
+                 const __grid_constant__ CUtensorMap tm_b48, const __grid_constant__ CUtensorMap tm_b64,
+                 TcParams p) {
+    using S = Smem<kPair>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *a_ring = sm + S::kAOff;
+    unsigned char *st_ring = sm + S::kStageOff;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
+    uint64_t *full = bars;                    // [kStages]
+    uint64_t *empty = full + kStages;         // [kStages]
+    uint64_t *afull = empty + kStages;        // [kAStages]
+    uint64_t *aempty = afull + kAStages;      // [kAStages]
+    uint64_t *accfull = aempty + kAStages;    // [2]
+    uint64_t *accempty = accfull + 2;         // [2]
+    uint64_t *drain = accempty + 2;           // [1] all issued MMAs complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kProdThreads + 1);
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&afull[i], kProdThreads);
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accfull[i], 1);
+            mbar_init(&accempty[i], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    pdl_wait();                      // union, buckets and activations of the previous kernels
+    pdl_launch_dependents();
+
+    const int nu = *p.n_union;
+    const int n_units = nu * p.n_tiles;
+    const int NC = p.n_chunks;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            uint32_t g = 0;
+            for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x) {
+                const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
+                const int e = p.union_ids[u];
+                const int off = p.offsets[u];
+                int m = p.offsets[u + 1] - off;
+                m = m > kNmax ? kNmax : m;
+                const int nb = (m + 15) >> 4;            // 1..4
+                const CUtensorMap *tb = nb <= 1 ? &tm_b16 : nb == 2 ? &tm_b32 : nb == 3 ? &tm_b48 : &tm_b64;
+                const uint32_t bbytes = (uint32_t)(nb < 1 ? 1 : nb) * 16 * kKc * 2;  // full box, OOB rows zero-filled
+                const int row = e * p.rows_per_expert + tile * kTile;
+                for (int c = 0; c < NC; ++c, ++g) {
+                    const int s = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
+                    unsigned char *stg = st_ring + s * S::kStageBytes;
+                    mbar_expect_tx(&full[s], S::kMats * kCodeBytes + bbytes);
+                    tma_load_2d(stg, &tm_a0, c * (kKc / 2), row, &full[s]);
+                    if (kPair) tma_load_2d(stg + kCodeBytes, &tm_a1, c * (kKc / 2), row, &full[s]);
+                    tma_load_2d(stg + S::kMats * kCodeBytes, tb, c * kKc, off, &full[s]);
+                }
+            }
+            // drain: every stage issued must have landed before the CTA exits
+            for (uint32_t k = (g > (uint32_t)kStages ? g - kStages : 0); k < g; ++k)
+                mbar_wait(&full[k % kStages], (k / kStages) & 1, abort_flag, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            uint32_t g = 0, i = 0;
+            bool issued = false;
+            for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
+                const int u = unit / p.n_tiles;
+                int m = p.offsets[u + 1] - p.offsets[u];
+                m = m > kNmax ? kNmax : m;
+                const int npad = ((m + 15) >> 4) << 4;
+                const uint32_t idesc = idesc_f16(kTile, npad < 16 ? 16 : npad);
+                const uint32_t b = i & 1;
+                if (!mbar_wait(&accempty[b], ((i >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem + b * kAccStride;
+                bool ok = true;
+                for (int c = 0; c < NC; ++c, ++g) {
+                    const int s = g % kStages, a = g % kAStages;
+                    if (!mbar_wait(&afull[a], (g / kAStages) & 1, abort_flag, p.status) ||
+                        !mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issued = true;
+                    const uint32_t abase = smem_u32(a_ring + a * S::kMats * kATileBytes);
+                    const uint32_t bbase = smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kKc / 16; ++kk) {
+                        const uint64_t bd = smem_desc_sw128(bbase + kk * 32);
+                        const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
+                        mma_f16(d0, smem_desc_sw128(abase + kk * 32), bd, idesc, acc);
+                        if (kPair)
+                            mma_f16(d0 + kUpCol, smem_desc_sw128(abase + kATileBytes + kk * 32), bd, idesc, acc);
+                    }
+                    mma_commit(&aempty[a]);
+                    mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&accfull[b]);
+            }
+            // every issued MMA must be complete before the TMEM is released
+            if (issued) {
+                mma_commit(drain);
+                mbar_wait(drain, 0, abort_flag, p.status);
+            }
+        }
+    } else if (warp < 8) {
+        // ---------------- dequant producers ----------------
+        const int r = tid >> 1, h = tid & 1;          // weight row in the tile, half of the chunk
+        uint32_t g = 0;
+        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x) {
+            const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
+            const int e = p.union_ids[u];
+            const size_t row = (size_t)e * p.rows_per_expert + tile * kTile + r;
+            const int NG = p.k_dim / kGroup;
+            bool ok = true;
+            for (int c = 0; c < NC; ++c, ++g) {
+                const int s = g % kStages, a = g % kAStages;
+                // scales/biases of this row and group (L1-cached: 16 groups share a sector)
+                const __half2 s0 = __half2half2(__float2half_rn(bf16_to_f32(p.s0[row * NG + c])));
+                const __half2 b0 = __half2half2(__float2half_rn(bf16_to_f32(p.b0[row * NG + c])));
+                __half2 s1 = s0, b1 = b0;
+                if (kPair) {
+                    s1 = __half2half2(__float2half_rn(bf16_to_f32(p.s1[row * NG + c])));
+                    b1 = __half2half2(__float2half_rn(bf16_to_f32(p.b1[row * NG + c])));
+                }
+                if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+                const unsigned char *stg = st_ring + s * S::kStageBytes;
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 32 + h * 16);
+                uint4 c1 = c0;
+                if (kPair) c1 = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + h * 16);
+                mbar_arrive(&empty[s]);                   // codes consumed
+                uint32_t q0[4][4], q1[4][4];
+                dequant_word(c0.x, s0, b0, q0[0]);
+                dequant_word(c0.y, s0, b0, q0[1]);
+                dequant_word(c0.z, s0, b0, q0[2]);
+                dequant_word(c0.w, s0, b0, q0[3]);
+                if (kPair) {
+                    dequant_word(c1.x, s1, b1, q1[0]);
+                    dequant_word(c1.y, s1, b1, q1[1]);
+                    dequant_word(c1.z, s1, b1, q1[2]);
+                    dequant_word(c1.w, s1, b1, q1[3]);
+                }
+                if (!mbar_wait(&aempty[a], ((g / kAStages) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+                unsigned char *at = a_ring + a * S::kMats * kATileBytes + r * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int phys = ((4 * h + j) ^ (r & 7)) * 16;
+                    *reinterpret_cast<uint4 *>(at + phys) = make_uint4(q0[j][0], q0[j][1], q0[j][2], q0[j][3]);
+                    if (kPair)
+                        *reinterpret_cast<uint4 *>(at + kATileBytes + phys) =
+                            make_uint4(q1[j][0], q1[j][1], q1[j][2], q1[j][3]);
+                }
+                fence_proxy_async();
+                mbar_arrive(&afull[a]);
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ---------------- epilogue (warps 8-11) ----------------
+        const int q = warp - kEpiWarp0;                // TMEM lane quarter
+        const int r = q * 32 + lane;                   // weight row in the tile
+        uint32_t i = 0;
+        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
+            const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
+            const int off = p.offsets[u];
+            int m = p.offsets[u + 1] - off;
+            if (m > kNmax) {
+                set_status(p.status, SMOE_ERR_DEVICE);
+                m = kNmax;
+            }
+            const uint32_t b = i & 1;
+            if (!mbar_wait(&accfull[b], (i >> 1) & 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * kAccStride;
+            const int orow = tile * kTile + r;
+            for (int n0 = 0; n0 < m; n0 += 16) {
+                float v0[16];
+                tmem_ld16(tbase + n0, v0);
+                if (kPair) {
+                    float v1[16];
+                    tmem_ld16(tbase + kUpCol + n0, v1);
+                    const int pos = perm8(orow);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (n0 + j < m)
+                            p.hout[(size_t)(off + n0 + j) * p.out_ld + pos] = __float2half_rn(silu_mul(v0[j], v1[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (n0 + j < m) p.oout[(size_t)(off + n0 + j) * p.out_ld + orow] = v0[j];
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&accempty[b]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// Bucket-ordered, 8-block-permuted fp16 copy of the normed inputs:
+// xperm[s] = perm(xn16[bucket_tok[s]]) for s < total, zero rows after.
+__global__ void __launch_bounds__(256) k_gather_xperm(PrefillArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int s = blockIdx.x;
+    const int total = a.offsets[*a.n_union];
+    const int D = a.D;
+    uint4 *dst = reinterpret_cast<uint4 *>(a.xperm + (size_t)s * D);
+    if (s >= total) {
+        for (int b = threadIdx.x; b < D / 8; b += blockDim.x) dst[b] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.xn16 + (size_t)a.bucket_tok[s] * D);
+    for (int b = threadIdx.x; b < D / 8; b += blockDim.x) {
+        const uint4 v = __ldcg(src + b);   // halves x0..x7 (two per word)
+        uint4 o;
+        // (x0,x4),(x1,x5),(x2,x6),(x3,x7)
+        o.x = __byte_perm(v.x, v.z, 0x5410);
+        o.y = __byte_perm(v.x, v.z, 0x7632);
+        o.z = __byte_perm(v.y, v.w, 0x5410);
+        o.w = __byte_perm(v.y, v.w, 0x7632);
+        dst[b] = o;
+    }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D map over a row-major [rows][cols] array of `esize`-byte elements.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t cols,
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * (cuuint64_t)esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kPair>
+cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap (&b)[4],
+                      const TcParams &p, cudaStream_t s, int grid) {
+    const size_t smem = Smem<kPair>::kBytes + 1024;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    return launch_kernel(k_prefill_tc<kPair>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
+                         b[1], b[2], b[3], p);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int D, int F) { return D % kTile == 0 && F % kTile == 0 && encode_fn() != nullptr; }
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
+    const int TK = a.T * a.K;
+    CUtensorMap mg, mu, md, mx[4], mh[4];
+    bool ok = make_map(&mg, a.gq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / 2, (uint64_t)a.E * a.F, kKc / 2, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&mu, a.uq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / 2, (uint64_t)a.E * a.F, kKc / 2, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&md, a.dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.F / 2, (uint64_t)a.E * a.D, kKc / 2, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    for (int i = 0; i < 4 && ok; ++i)
+        ok = make_map(&mx[i], a.xperm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.D, TK, kKc, 16 * (i + 1),
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+             make_map(&mh[i], a.hbuf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.F, TK, kKc, 16 * (i + 1),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return cudaErrorInvalidValue;
+
+    cudaError_t e = launch_kernel(k_gather_xperm, dim3(TK), dim3(256), 0, s, true, a);
+    if (e != cudaSuccess) return e;
+    const int grid = a.num_sms;
+    TcParams gu{};
+    gu.n_tiles = a.F / kTile;
+    gu.n_chunks = a.D / kKc;
+    gu.rows_per_expert = a.F;
+    gu.k_dim = a.D;
+    gu.out_ld = a.F;
+    gu.n_union = a.n_union;
+    gu.union_ids = a.union_ids;
+    gu.offsets = a.offsets;
+    gu.s0 = a.gs; gu.b0 = a.gb; gu.s1 = a.us; gu.b1 = a.ub;
+    gu.hout = a.hbuf;
+    gu.status = a.status;
+    if ((e = launch_tc<true>(mg, mu, mx, gu, s, grid)) != cudaSuccess) return e;
+    TcParams dn = gu;
+    dn.n_tiles = a.D / kTile;
+    dn.n_chunks = a.F / kKc;
+    dn.rows_per_expert = a.D;
+    dn.k_dim = a.F;
+    dn.out_ld = a.D;
+    dn.s0 = a.ds; dn.b0 = a.db; dn.s1 = nullptr; dn.b1 = nullptr;
+    dn.hout = nullptr;
+    dn.oout = a.obuf;
+    return launch_tc<false>(md, md, mh, dn, s, grid);
+}
+
+}  // namespace smoe

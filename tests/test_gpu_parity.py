@@ -281,3 +281,18 @@ def test_prefill_all_tokens_one_bucket(smoe, orc):
     yh = bf16_f64(host(y))
     assert rel_l2(yh[0], ref["y"]) <= TOL
     assert np.all(yh == yh[0])
+
+
+def test_alternate_engines_in_subprocess(smoe):
+    """The CUDA-core prefill engine (SMOE_PREFILL_PATH=simt) and the three-kernel
+    decode engine (SMOE_DECODE_PATH=split) pass the same parity cases as the
+    default engines (tensor-core prefill, one-kernel decode layer)."""
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, SMOE_PREFILL_PATH="simt", SMOE_DECODE_PATH="split")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+                        "tests/test_gpu_parity.py", "-k", "(prefill or decode) and not subprocess"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
