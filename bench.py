@@ -134,6 +134,22 @@ def traffic_from_profile(name, source_files):
     return float(m.group(1))
 
 
+def replica_rate(units_per_rank, elapsed_ms, device=None):
+    """Whole-job rate of N independent replicas: every rank processed
+    units_per_rank units; the job took the slowest rank's time (max over ranks,
+    one all-reduce that is timing only, not data path).  Returns (rate in
+    units/s, job ms).  Without an initialised process group: one replica."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        n = dist.get_world_size()
+        ms = float(t.item())
+    else:
+        n, ms = 1, float(elapsed_ms)
+    return units_per_rank * n / (ms / 1e3), ms
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -386,13 +402,8 @@ def our_arm(args):
     with Clocks(dev.index) as ck:
         ms_tok, ms_total = time_decode(stack, states, args.steps, args.warmup, batch)
     clocks = ck.summary()
-    if ws_ > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-        ms_tok = ms_total / args.steps
-    value = args.steps * ws_ / (ms_total / 1e3)
+    value, ms_total = replica_rate(args.steps, ms_total, dev if ws_ > 1 else None)
+    ms_tok = ms_total / args.steps
     bytes_token = L30 * (K * expert_bytes(D30, F30) + E * D30 * 2)
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": ws_,

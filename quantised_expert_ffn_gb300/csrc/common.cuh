@@ -116,6 +116,14 @@ __device__ __forceinline__ uint16_t rms_apply(uint16_t x, float inv, uint16_t ga
     return f32_to_bf16(bf16_to_f32(x) * inv * bf16_to_f32(gain));
 }
 
+// Nanoseconds of the global timer (bounds every wait of the persistent kernels).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;   // 200 ms: far beyond any legitimate wait
+
 // Programmatic dependent launch controls (no-ops when launched without PDL).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -223,11 +223,14 @@ __global__ void __launch_bounds__(kThreads) k_decode_down(DecodeArgs a) {
 
     const int items = K * rows;
     const float4 *hs4 = reinterpret_cast<const float4 *>(hs);
-    for (int q = S; q < items; q += 32) {
-        const int i = q / rows, dl = q - i * rows;
+    // warp-uniform trip count: every lane reaches the shuffles below
+    for (int base = warp * 4; base < items; base += 32) {
+        const int q = base + (S - warp * 4);
+        const bool live = q < items;
+        const int i = live ? q / rows : 0, dl = live ? q - i * rows : 0;
         const int e = eid[i];
         float acc = 0.f;
-        if (e >= 0) {
+        if (live && e >= 0) {
             const size_t row = (size_t)e * D + d0 + dl;
             const uint8_t *rp = a.dq + row * (F / 2);
             for (int mb = 0; mb < MC; mb += 4) {
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_down(DecodeArgs a) {
         acc += __shfl_xor_sync(0xffffffffu, acc, 4);
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        if (s8 == 0) {
+        if (live && s8 == 0) {
             os[i * R + dl] = acc;
             if (a.expert_out) a.expert_out[(size_t)i * D + d0 + dl] = acc;
         }

@@ -39,14 +39,15 @@ namespace {
 constexpr int kCompute = 256;          // warps 0-7
 constexpr int kThreadsF = kCompute + 32;   // + producer warp 8
 constexpr int kSlots = 3;
-constexpr long long kSpin = 1ll << 22;
 
 // ---------------------------------------------------------------- primitives
 
 __device__ __forceinline__ uint32_t su32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void bar_compute() { asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory"); }
+// Named barrier of the 256 compute threads.  The non-aligned form: lanes of a
+// warp may arrive from divergent paths (e.g. thread 0 leaving a spin).
+__device__ __forceinline__ void bar_compute() { asm volatile("barrier.sync 1, %0;" ::"n"(kCompute) : "memory"); }
 
 __device__ __forceinline__ void mb_init(uint64_t *b, uint32_t n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
@@ -68,9 +69,15 @@ __device__ __forceinline__ bool mb_try(uint64_t *b, uint32_t par) {
         : "memory");
     return ok;
 }
+// Wait for the phase of parity `par`, bounded in wall time.
 __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t par, int32_t *status) {
-    for (long long i = 0; i < kSpin; ++i)
-        if (mb_try(b, par)) return true;
+    if (mb_try(b, par)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mb_try(b, par)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) break;
+    }
     set_status(status, SMOE_ERR_TIMEOUT);
     return false;
 }
@@ -102,15 +109,18 @@ __device__ __forceinline__ void grid_sync(uint32_t *bar, int32_t *status) {
             __threadfence();
             atomicAdd(bar + 1, 1u);
         } else {
-            long long i = 0;
-            for (; i < kSpin; ++i) {
-                if (ld_acquire_u32(bar + 1) != gen) break;
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_u32(bar + 1) == gen) {
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    set_status(status, SMOE_ERR_TIMEOUT);
+                    break;
+                }
                 __nanosleep(32);
             }
-            if (i == kSpin) set_status(status, SMOE_ERR_TIMEOUT);
         }
         __threadfence();
     }
+    __syncwarp();
     bar_compute();
 }
 
@@ -523,13 +533,16 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             mb_wait(&full[s], (g / kSlots) & 1, a.status);
             const unsigned char *slot = ring + s * a.slot_bytes;
             const uint32_t cb = rows * (F / 2), sb = rows * FG * 2;
-            for (int q = S; q < ne * rows; q += 32) {
-                const int qi = q / rows, r = q - qi * rows, i = i0 + qi;
+            // warp-uniform trip count: every lane reaches the shuffles below
+            for (int base = warp * 4; base < ne * rows; base += 32) {
+                const int q = base + (S - warp * 4);
+                const bool live = q < ne * rows;
+                const int qi = live ? q / rows : 0, r = live ? q - qi * rows : 0, i = i0 + qi;
                 const unsigned char *rp = slot + qi * cb + r * (F / 2);
                 const uint16_t *sr = reinterpret_cast<const uint16_t *>(slot + ne * cb + qi * 2 * sb) + r * FG;
                 const uint16_t *br = sr + rows * FG;
                 float acc = 0.f;
-                for (int m = 0; m < MC; ++m) {
+                for (int m = 0; m < MC && live; ++m) {
                     const int c = s8 + 8 * m;
                     if (c >= FC) break;
                     const uint4 cv = *reinterpret_cast<const uint4 *>(rp + c * 16);
@@ -545,7 +558,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 acc += __shfl_xor_sync(0xffffffffu, acc, 4);
                 acc += __shfl_xor_sync(0xffffffffu, acc, 2);
                 acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                if (s8 == 0) os[i * a.rows_max + r] = acc;
+                if (live && s8 == 0) os[i * a.rows_max + r] = acc;
             }
             __syncwarp();
             if (lane == 0) mb_arrive(&empty[s]);

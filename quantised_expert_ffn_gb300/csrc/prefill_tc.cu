@@ -58,7 +58,6 @@ constexpr uint32_t kUpCol = 128;
 constexpr int kCodeBytes = kTile * kKc / 2;          // 4 KB of codes per matrix per stage
 constexpr int kATileBytes = kTile * kKc * 2;         // 16 KB fp16 A tile
 constexpr int kBTileBytes = kNmax * kKc * 2;         // 8 KB fp16 B tile (up to 64 rows)
-constexpr long long kSpinLimit = 1ll << 22;
 
 struct TcParams {
     int n_tiles;            // 128-row tiles per expert
@@ -105,12 +104,17 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete; false on timeout or abort.
+// Wait for the phase of `parity` to complete, bounded in wall time; false on
+// timeout (which also raises the CTA's abort flag) or when another role aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag,
                                           int32_t *status) {
-    for (long long i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try(b, parity)) return true;
-        if ((i & 1023) == 1023 && *abort_flag) return false;
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try(b, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) break;
     }
     *abort_flag = 1;
     set_status(status, SMOE_ERR_TIMEOUT);
@@ -414,7 +418,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 m = kNmax;
             }
             const uint32_t b = i & 1;
-            if (!mbar_wait(&accfull[b], (i >> 1) & 1, abort_flag, p.status)) break;
+            const bool got = mbar_wait(&accfull[b], (i >> 1) & 1, abort_flag, p.status);
+            __syncwarp();                               // tcgen05.ld is warp-aligned
+            if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * kAccStride;
             const int orow = tile * kTile + r;
@@ -440,10 +446,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
 
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) {
+        __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
 }
