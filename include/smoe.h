@@ -187,6 +187,28 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
                            int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
                            smoe_stream stream);
 
+/* Decode without a workspace.  The pages have no counterpart of this call:
+ * it exists for callers that cannot allocate device memory when they run a
+ * layer -- code inside a CUDA graph capture (an allocation cannot be
+ * captured), real-time loops whose latency budget rules out the device-wide
+ * synchronisation an allocation may cause, and plug-ins whose host program
+ * owns all device memory through its own pool.
+ * Computes exactly what smoe_moe_decode computes (same kernels); the scratch
+ * lives in a fixed device array of the library, SMOE_DECODE_NOALLOC_MAX_BYTES
+ * bytes, that every GPU which loads the library holds until the process
+ * exits.  A layer whose smoe_workspace_bytes(layer, 1) exceeds that size is
+ * rejected with SMOE_ERR_WORKSPACE and nothing is enqueued.  The first call on
+ * a device looks up the array's device address (once, with that device
+ * current); make that first call before any stream capture.  Every call
+ * zeroes the array's status word and counters (a 1 KiB cudaMemsetAsync on
+ * `stream`) and allocates nothing.  All calls share the one array: calls that
+ * overlap on the GPU (different streams, no ordering) race and give
+ * undefined results.  x, y bf16 [D] (y may alias x); idx_out int32 [k] and
+ * w_out fp32 [k] optional. */
+#define SMOE_DECODE_NOALLOC_MAX_BYTES (512u * 1024u)
+int smoe_moe_decode_noalloc(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
+                            int32_t *idx_out_opt, float *w_out_opt, smoe_stream stream);
+
 /* A static string naming a status code. */
 const char *smoe_status_string(int status);
 

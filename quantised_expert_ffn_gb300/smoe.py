@@ -71,6 +71,7 @@ def _load():
         "smoe_moe_ffn_decode": (I, [LP, P, P, P, P, P, P, Z, P]),
         "smoe_moe_prefill_chunk": (I, [LP, P, I, P, P, P, P, Z, P]),
         "smoe_status_string": (ctypes.c_char_p, [I]),
+        "smoe_moe_decode_noalloc": (I, [LP, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -82,7 +83,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_status",
             "smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_ffn_decode",
-            "smoe_moe_prefill_chunk", "smoe_status_string")
+            "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc")
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -180,3 +181,14 @@ def smoe_moe_prefill_chunk(layer: Layer, x, T, y, idx_out=None, w_out=None, ws=N
     _check(_lib.smoe_moe_prefill_chunk(layer.ref, _p(x), int(T), _p(y), _p(idx_out), _p(w_out),
                                        _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "smoe_moe_prefill_chunk")
+
+
+SMOE_DECODE_NOALLOC_MAX_BYTES = 512 * 1024
+
+
+def smoe_moe_decode_noalloc(layer: Layer, x, y, idx_out=None, w_out=None, stream=None):
+    """Decode one token with the library's fixed device scratch instead of a
+    workspace (for callers that cannot allocate device memory, e.g. inside a
+    graph capture); see include/smoe.h."""
+    _check(_lib.smoe_moe_decode_noalloc(layer.ref, _p(x), _p(y), _p(idx_out), _p(w_out),
+                                        _stream(stream)), "smoe_moe_decode_noalloc")

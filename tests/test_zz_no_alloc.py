@@ -1,0 +1,58 @@
+"""smoe_moe_decode_noalloc: decode without a workspace, for callers that cannot
+allocate device memory (inside a graph capture, latency-bound serving loops,
+plug-ins whose host owns the device memory).  Its output must match the
+workspace entry point's, call after call: the fixed scratch keeps the previous
+call's contents, so two calls in a row are checked.  This file is collected
+last so that a failure here comes after every other test has run."""
+import numpy as np
+import pytest
+import torch
+
+from quantised_expert_ffn_gb300 import synth
+from tests.util import bf16_f64, host, rel_l2
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def smoe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantised_expert_ffn_gb300 import build
+    build.build()
+    from quantised_expert_ffn_gb300 import smoe as m
+    return m
+
+
+@pytest.mark.parametrize("D,E,K,F", [(2048, 128, 8, 768), (4096, 128, 8, 1536), (128, 16, 4, 128)])
+def test_noalloc_matches_workspace_decode_twice(smoe, D, E, K, F):
+    W = synth.layer_weights(D, E, F, K, seed=4242, device="cuda", rms_norm=True)
+    L = smoe.Layer(W)
+    assert smoe.smoe_workspace_bytes(L, 1) <= smoe.SMOE_DECODE_NOALLOC_MAX_BYTES
+    ws = smoe.workspace(L, 1)
+    xs = synth.hidden(2, D, seed=99, device="cuda")
+    for t in range(2):                                   # two calls in a row
+        y_ref = torch.empty_like(xs[t])
+        idx_ref = torch.empty(K, dtype=torch.int32, device="cuda")
+        w_ref = torch.empty(K, dtype=torch.float32, device="cuda")
+        smoe.smoe_moe_decode(L, xs[t], y_ref, idx_ref, w_ref, None, ws)
+        y = torch.empty_like(xs[t])
+        idx = torch.full((K,), -1, dtype=torch.int32, device="cuda")
+        w = torch.zeros(K, dtype=torch.float32, device="cuda")
+        smoe.smoe_moe_decode_noalloc(L, xs[t], y, idx, w)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, idx_ref)
+        np.testing.assert_allclose(host(w), host(w_ref), rtol=1e-6)
+        assert rel_l2(bf16_f64(host(y)), bf16_f64(host(y_ref))) <= TOL
+    assert smoe.smoe_read_device_status(ws) == 0
+
+
+def test_noalloc_rejects_layers_beyond_its_scratch(smoe):
+    W = synth.layer_weights(8192, 16, 2048, 8, seed=1, device="cuda")
+    L = smoe.Layer(W)
+    assert smoe.smoe_workspace_bytes(L, 1) > smoe.SMOE_DECODE_NOALLOC_MAX_BYTES
+    x = torch.zeros(8192, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(smoe.SmoeError) as e:
+        smoe.smoe_moe_decode_noalloc(L, x, torch.empty_like(x))
+    assert e.value.status == smoe.SMOE_ERR_WORKSPACE
