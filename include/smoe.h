@@ -209,6 +209,10 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
 int smoe_moe_decode_noalloc(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
                             int32_t *idx_out_opt, float *w_out_opt, smoe_stream stream);
 
+/* Name of the last CUDA error behind an SMOE_ERR_CUDA returned on this host
+ * thread ("cudaSuccess" if none), for diagnostics. */
+const char *smoe_last_cuda_error(void);
+
 /* A static string naming a status code. */
 const char *smoe_status_string(int status);
 

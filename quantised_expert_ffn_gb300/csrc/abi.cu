@@ -6,6 +6,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,13 +32,13 @@ WsLayout ws_layout(const smoe_layer &L, int T) {
     size_t p = 0;
     o.status = p;      p += kAlign;                       // int32 status word (+ padding)
     o.counters = p;    p = up(p + kMaxChunk * 4);
-    o.gbar = p;        p = up(p + 8);                    // grid barrier {count, generation}
+    o.gbar = p;        p = up(p + 8);                    // grid barrier arrival counter (own line)
     o.idx = p;         p = up(p + TK * 4);
     o.w = p;           p = up(p + TK * 4);
     o.logits = p;      p = up(p + (size_t)T * E * 4);
     o.xn = p;          p = up(p + (size_t)T * D * 2);
     o.xn16 = p;        p = up(p + (size_t)T * D * 2);
-    o.h = p;           p = up(p + K * F * 4);
+    o.h = p;           p = up(p + std::max(K * F, fused_h_floats((int)F, (int)K)) * 4);
     o.n_union = p;     p = up(p + 4);
     o.union_ids = p;   p = up(p + E * 4);
     o.offsets = p;     p = up(p + (E + 1) * 4);
@@ -87,7 +89,13 @@ T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SMOE_OK;
+    g_last_cuda_error = e;
+    return SMOE_ERR_CUDA;
+}
 
 // Decode engine: 1 = fused one-kernel layer, 0 = three kernels (router, gate/up,
 // down).  SMOE_DECODE_PATH=split selects the latter (cross-check).
@@ -205,7 +213,7 @@ static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int
     f.dq = L.down_q; f.ds = L.down_s; f.db = L.down_b;
     f.logits = at<float>(ws, o.logits);
     f.h = at<float>(ws, o.h);
-    f.bar = at<uint32_t>(ws, o.gbar);
+    f.gctr = at<unsigned long long>(ws, o.gbar);
     f.status = at<int32_t>(ws, o.status);
     f.idx_out = idx_out;
     f.w_out = w_out;
@@ -216,7 +224,8 @@ static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int
         return cuda_status(launch_decode_layer(f, s, idx_in == nullptr));
     if (!idx_in) {
         RouteArgs r = route_args(L, x, ws, o, idx_out, w_out, nullptr, nullptr, nullptr);
-        if (launch_route_topk(r, 1, s, true) != cudaSuccess) return SMOE_ERR_CUDA;
+        const int st = cuda_status(launch_route_topk(r, 1, s, true));
+        if (st != SMOE_OK) return st;
         idx_in = idx_out;
         w_in = w_out;
     }
@@ -237,7 +246,8 @@ static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int
     d.y = y;
     d.expert_out = expert_out;
     d.status = at<int32_t>(ws, o.status);
-    if (launch_decode_gateup(d, s, true) != cudaSuccess) return SMOE_ERR_CUDA;
+    const int st = cuda_status(launch_decode_gateup(d, s, true));
+    if (st != SMOE_OK) return st;
     return cuda_status(launch_decode_down(d, s, true));
 }
 
@@ -283,13 +293,12 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     float *w = w_out_opt ? w_out_opt : at<float>(ws, o.w);
     RouteArgs r = route_args(L, x, ws, o, idx, w, nullptr, at<smoe_bf16>(ws, o.xn),
                              at<__half>(ws, o.xn16));
-    cudaError_t e = launch_route_topk(r, T, s, true);
-    if (e != cudaSuccess) return SMOE_ERR_CUDA;
+    if ((st = cuda_status(launch_route_topk(r, T, s, true))) != SMOE_OK) return st;
     UnionArgs u{idx, w, T, L.top_k, L.n_experts, at<int32_t>(ws, o.union_ids),
                 at<int32_t>(ws, o.n_union), at<int32_t>(ws, o.offsets),
                 at<int32_t>(ws, o.bucket_tok), at<int32_t>(ws, o.bucket_rank),
                 at<float>(ws, o.bucket_w), at<int32_t>(ws, o.status), at<int32_t>(ws, o.slot_of)};
-    if ((e = launch_expert_union(u, s, true)) != cudaSuccess) return SMOE_ERR_CUDA;
+    if ((st = cuda_status(launch_expert_union(u, s, true))) != SMOE_OK) return st;
     PrefillArgs p{};
     p.x = x;
     p.T = T;
@@ -315,11 +324,13 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     p.status = at<int32_t>(ws, o.status);
     p.num_sms = device_sm_count();
     if (prefill_path() == 1 && prefill_tc_supported(p.D, p.F)) {
-        if (launch_prefill_tc(p, s) != cudaSuccess) return SMOE_ERR_CUDA;
+        if ((st = cuda_status(launch_prefill_tc(p, s))) != SMOE_OK) return st;
         return cuda_status(launch_prefill_combine(p, s, true));
     }
     return cuda_status(launch_prefill_simt(p, at<smoe_bf16>(ws, o.xn), at<float>(ws, o.h32), s, true));
 }
+
+const char *smoe_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 const char *smoe_status_string(int status) {
     switch (status) {

@@ -124,6 +124,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;   // 200 ms: far beyond any legitimate wait
 
+// mbarrier phase test that suspends the calling thread in hardware (up to
+// `hint_ns`) until the phase completes, instead of returning at once: waiting
+// threads then take no issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar_smem, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar_smem), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kSuspendHintNs = 20000;   // 20 us per try; the wall-clock bound still applies
+
 // Programmatic dependent launch controls (no-ops when launched without PDL).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -9,26 +9,27 @@
 // (weighted sum into the residual).
 //
 // At batch 1 a layer is a chain of three dependent steps (route -> gate/up ->
-// down) over ~22 MB (30B shape) to ~86 MB (235B shape) of weights, i.e. a few
-// microseconds of HBM time, so the cost is latency.  One CTA per SM runs the
-// whole layer with two grid-wide barriers (device-scope counter and
-// generation word, bounded spin):
+// down) over ~22 MB (30B shape) to ~86 MB (235B shape) of weights, a few
+// microseconds of HBM time, so latency is the cost.  One CTA per SM runs the
+// whole layer with two grid-wide barriers (one 64-bit arrival counter that
+// only grows, on its own cache line; wall-clock-bounded polling):
 //   phase 0  CTA c < E loads router row c before it waits for the previous
-//            kernel (programmatic dependent launch), then normalises x (all
-//            CTAs, fp32, the same arithmetic as the stand-alone router) and
-//            writes logit c;                                     -- barrier 1
-//   phase 1  every CTA ranks the E logits itself (no second launch), and a
-//            producer warp streams this CTA's gate/up rows AND its down rows
-//            with bulk async copies (cp.async.bulk, the TMA engine) into a
-//            ring of shared-memory slots; 8 compute warps turn gate/up rows
-//            into h = SiLU(g)*u (fp32, to global);                -- barrier 2
-//   phase 2  down rows (already resident in shared memory) times h, combined
-//            in rank order with the residual: y = x + sum_i w_i o_i.
-// The per-row arithmetic is that of decode.cu: a code q becomes the float
-// 128+q by one byte permute; per 32-code chunk s*sum((128+q)x) + (b-128s)*sum(x).
+//            kernel (programmatic dependent launch), normalises x (fp32, the
+//            stand-alone router's arithmetic) and writes logit c;  -- barrier
+//   phase 1  every CTA ranks the E logits itself; a producer warp streams this
+//            CTA's gate/up rows and then its down rows with 1-D bulk async
+//            copies (cp.async.bulk, the TMA engine) into a 4-slot shared-
+//            memory ring; 16 compute warps turn gate/up rows into h = SiLU(g)*u
+//            and store it, fp32, straight into the layout the down phase
+//            reads;                                                -- barrier
+//   phase 2  one bulk copy brings all of h into shared memory; the down rows
+//            (mostly resident already) times h, combined in rank order with
+//            the residual: y = x + sum_i w_i o_i.
+// Per-row arithmetic as in decode.cu: a code q becomes the float 128+q by one
+// byte permute; per 32-code chunk s*sum((128+q)x) + (b-128s)*sum(x).
 //
-// Every wait (mbarrier or grid barrier) is bounded; on timeout the kernel
-// records SMOE_ERR_TIMEOUT in the status word and runs to completion.
+// Every wait (mbarrier or grid barrier) is bounded in wall time; on timeout
+// the kernel records SMOE_ERR_TIMEOUT in the status word and runs to the end.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -36,17 +37,23 @@ namespace smoe {
 
 namespace {
 
-constexpr int kCompute = 256;          // warps 0-7
-constexpr int kThreadsF = kCompute + 32;   // + producer warp 8
+// 14 compute warps + 1 producer: 15 warps put at most 4 on each of the SM's
+// four schedulers, so each thread may hold 128 registers (the per-scheduler
+// register file is 16K), enough to keep a lane's 64 activations resident.
+constexpr int kWarpsC = 14;                    // compute warps
+constexpr int kCompute = kWarpsC * 32;
+constexpr int kThreadsF = kCompute + 32;       // + producer warp
 constexpr int kSlots = 3;
+constexpr int kSlotMax = 48 * 1024 + 512;     // largest ring slot
+constexpr int kMaxGuRows = 128;                // gate/up row pairs per CTA
 
 // ---------------------------------------------------------------- primitives
 
 __device__ __forceinline__ uint32_t su32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-// Named barrier of the 256 compute threads.  The non-aligned form: lanes of a
-// warp may arrive from divergent paths (e.g. thread 0 leaving a spin).
+// Named barrier of the compute threads; the non-aligned form, so lanes of a
+// warp may arrive from divergent paths (thread 0 leaving a spin).
 __device__ __forceinline__ void bar_compute() { asm volatile("barrier.sync 1, %0;" ::"n"(kCompute) : "memory"); }
 
 __device__ __forceinline__ void mb_init(uint64_t *b, uint32_t n) {
@@ -69,19 +76,26 @@ __device__ __forceinline__ bool mb_try(uint64_t *b, uint32_t par) {
         : "memory");
     return ok;
 }
-// Wait for the phase of parity `par`, bounded in wall time.
+// Wait for the phase of parity `par`, bounded in wall time; the thread sleeps
+// in hardware between tries.
 __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t par, int32_t *status) {
     if (mb_try(b, par)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mb_try(b, par)) return true;
+        if (mbar_try_suspend(su32(b), par, kSuspendHintNs)) return true;
         if (global_ns() - t0 > kWaitLimitNs) break;
     }
     set_status(status, SMOE_ERR_TIMEOUT);
     return false;
 }
-// 1-D bulk copy global -> shared, completion counted on `bar` (sizes, addresses: 16-byte multiples)
+// Compute warps wait on a barrier: one lane polls, then every lane observes the
+// completed phase (so each lane's later shared-memory reads are ordered after it).
+__device__ __forceinline__ void warp_wait(uint64_t *b, uint32_t par, int32_t *status) {
+    if ((threadIdx.x & 31) == 0) mb_wait(b, par, status);
+    __syncwarp();
+    mb_try(b, par);
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (16-byte multiples)
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -90,35 +104,29 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid-wide barrier for the compute warps of every CTA (all CTAs resident:
-// one per SM).  bar[0] counts arrivals, bar[1] is the generation.
-__device__ __forceinline__ void grid_sync(uint32_t *bar, int32_t *status) {
+// Grid-wide barrier over the compute warps of all CTAs (one CTA per SM, all
+// resident).  `ctr` only grows: an arrival that returns `prev` belongs to the
+// barrier instance that ends at the next multiple of gridDim.x.
+__device__ __forceinline__ void grid_sync(unsigned long long *ctr, int32_t *status) {
     bar_compute();
     if (threadIdx.x == 0) {
-        const uint32_t gen = ld_acquire_u32(bar + 1);
-        __threadfence();
-        const uint32_t prev = atomicAdd(bar, 1u);
-        if (prev == gridDim.x - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
+        const unsigned long long G = gridDim.x;
+        unsigned long long prev, v;
+        asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(prev) : "l"(ctr) : "memory");
+        const unsigned long long target = (prev / G + 1) * G;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if (v < target) {
             const uint64_t t0 = global_ns();
-            while (ld_acquire_u32(bar + 1) == gen) {
+            while (true) {
+                __nanosleep(40);
+                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+                if (v >= target) break;
                 if (global_ns() - t0 > kWaitLimitNs) {
                     set_status(status, SMOE_ERR_TIMEOUT);
                     break;
                 }
-                __nanosleep(32);
             }
         }
-        __threadfence();
     }
     __syncwarp();
     bar_compute();
@@ -131,10 +139,20 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// sum_k (128+q_k) x_k over the 32 codes of a 16-byte chunk, two independent chains
+__device__ __forceinline__ float dot32(uint4 c, const float4 (&x)[8]) {
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+    dot8(c.x, x[0], x[1], a0);
+    dot8(c.y, x[2], x[3], a1);
+    dot8(c.z, x[4], x[5], a0);
+    dot8(c.w, x[6], x[7], a1);
+    return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
 // ---------------------------------------------------------------- work lists
 
-// Gate/up: CTA c owns row pairs [P*c/G, P*(c+1)/G) of the K*F (slot, row) pairs;
-// an item is up to R consecutive rows of one expert slot.
+// Gate/up: CTA c owns row pairs [P*c/G, P*(c+1)/G) of the K*F (slot, row)
+// pairs; an item is up to r_gu consecutive rows of one expert slot.
 struct GuIt {
     int i, j0, n;   // expert slot, first row, rows
 };
@@ -144,7 +162,7 @@ __device__ __forceinline__ bool gu_item(const FusedArgs &a, int idx, GuIt &it) {
     const int p1 = (int)(P * (blockIdx.x + 1) / gridDim.x);
     for (int k = 0; p < p1; ++k) {
         const int i = p / a.F, j = p - i * a.F;
-        int n = min(a.r_gu, min(p1 - p, a.F - j));
+        const int n = min(a.r_gu, min(p1 - p, a.F - j));
         if (k == idx) {
             it = {i, j, n};
             return true;
@@ -154,12 +172,83 @@ __device__ __forceinline__ bool gu_item(const FusedArgs &a, int idx, GuIt &it) {
     return false;
 }
 
-// Down: CTA c owns output rows [d0, d1) (multiples of a.dn_gran); an item is
-// up to a.e_dn consecutive expert slots of those rows.
+// Down: CTA c owns output rows [d0, d1), multiples of a.dn_gran rows (so each
+// row block's scale block starts 16-byte aligned); an item is up to a.e_dn
+// consecutive expert slots of those rows.
 __device__ __forceinline__ void dn_rows(const FusedArgs &a, int &d0, int &d1) {
     const int units = a.D / a.dn_gran;
     d0 = (int)((long long)units * blockIdx.x / gridDim.x) * a.dn_gran;
     d1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x) * a.dn_gran;
+}
+
+// Position of h[i][f] in the down phase's layout: chunk c = f/32 is handled by
+// lane s8 = c%8 of a subgroup in round m = c/8; float4 k = (f%32)/4 of the
+// chunk sits at ((i*MC + m)*8 + k)*8 + s8 (conflict-free 16-byte reads).
+__device__ __forceinline__ int h_pos(int i, int f, int MC) {
+    const int c = f >> 5, k = (f & 31) >> 2;
+    return ((((i * MC + (c >> 3)) * 8 + k) * 8 + (c & 7)) << 2) + (f & 3);
+}
+
+// ---------------------------------------------------------------- down phase
+
+// One down item (experts i0..i0+ne-1, this CTA's `rows` rows) from ring slot
+// `slot`: an SG-lane subgroup takes RU rows of one expert; lane l handles chunks
+// l, l+SG, l+2SG, ... of each row, so one 32-value h load serves RU rows.  The
+// sums of the item's (expert, row) pairs go to os[i][r].
+template <int SG, int RU>
+__device__ __forceinline__ void down_item(const unsigned char *slot, int i0, int ne, int rows, int F, int MC,
+                                          const float4 *hs4, const float *hc, float *os, int rows_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int l = lane % SG, sub = lane / SG;
+    constexpr int kSubPerWarp = 32 / SG;
+    const int FC = F / 32, FG = F / kGroup;
+    const uint32_t cb = rows * (F / 2), sb = rows * FG * 2;
+    const int RP = (rows + RU - 1) / RU;
+    const int units = ne * RP;
+    // warp-uniform trip count: every lane reaches the shuffles below
+    for (int base = warp * kSubPerWarp; base < units; base += kWarpsC * kSubPerWarp) {
+        const int q = base + sub;
+        const bool live = q < units;
+        const int qi = live ? q / RP : 0, rp = live ? q - qi * RP : 0, i = i0 + qi;
+        float acc[RU];
+        const unsigned char *rowp[RU];
+        const uint16_t *srp[RU], *brp[RU];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            acc[u] = 0.f;
+            const int r = min(rp * RU + u, rows - 1);            // a missing last row repeats a real one
+            rowp[u] = slot + qi * cb + r * (F / 2);
+            srp[u] = reinterpret_cast<const uint16_t *>(slot + ne * cb + qi * 2 * sb) + r * FG;
+            brp[u] = srp[u] + rows * FG;
+        }
+        if (live) {
+            for (int c = l; c < FC; c += SG) {
+                const float4 *hv = hs4 + ((i * MC + (c >> 3)) * 8) * 8 + (c & 7);
+                float4 hq[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) hq[k] = hv[k * 8];
+                const float H = hc[(i * MC + (c >> 3)) * 8 + (c & 7)];
+                uint4 cv[RU];
+#pragma unroll
+                for (int u = 0; u < RU; ++u) cv[u] = *reinterpret_cast<const uint4 *>(rowp[u] + c * 16);
+#pragma unroll
+                for (int u = 0; u < RU; ++u) {
+                    const float A = dot32(cv[u], hq);
+                    const float sc = bf16_to_f32(srp[u][c >> 1]), bi = bf16_to_f32(brp[u][c >> 1]);
+                    acc[u] += sc * A + (bi - 128.f * sc) * H;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < RU; ++u)
+#pragma unroll
+            for (int o = SG / 2; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+        if (live && l == 0) {
+#pragma unroll
+            for (int u = 0; u < RU; ++u)
+                if (rp * RU + u < rows) os[i * rows_max + rp * RU + u] = acc[u];
+        }
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -171,28 +260,30 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     const int NC = D / 32;                       // 32-code chunks of a gate/up row
     const int NCP = (NC + 63) / 64;              // passes of 64 chunks (2 per lane)
     const int FC = F / 32;                       // chunks of a down row
-    const int MC = (FC + 7) / 8;                 // chunks per lane of an 8-lane subgroup
+    const int MC = (FC + 7) / 8;                 // chunk rounds of an 8-lane subgroup
     unsigned char *ring = sm;
-    float *u_region = reinterpret_cast<float *>(sm + a.ring_bytes);       // xs+xc | hs+hc
-    float *xs = u_region;                        // NCP*64*8 float4 = NCP*2048 floats
+    float *u_region = reinterpret_cast<float *>(sm + a.ring_bytes);       // xs+xc | hs
+    float *xs = u_region;                        // NCP*64*8 float4
     float *xc = xs + NCP * 2048;                 // NCP*64 chunk sums
-    float *hs = u_region;                        // K*MC*64 float4 = K*MC*256 floats
-    float *hc = hs + K * MC * 256;               // K*MC*8
+    float *hs = u_region;                        // K*MC*256 floats
+    float *hc = hs + K * MC * 256;               // K*MC*8 chunk sums of h
     uint16_t *xraw = reinterpret_cast<uint16_t *>(sm + a.ring_bytes + a.union_bytes);   // [D]
     float *os = reinterpret_cast<float *>(xraw + D);                                 // [K][rows_max]
-    __shared__ uint64_t full[kSlots], empty[kSlots], idx_ready;
-    __shared__ float red[8];
-    __shared__ uint32_t keys[kMaxExperts];
+    __shared__ uint64_t full[kSlots], empty[kSlots], idx_ready, h_ready;
+    __shared__ float red[kWarpsC];
+    __shared__ __align__(16) unsigned long long keys[kMaxExperts];
     __shared__ float lsel[kMaxTopK], wsel[kMaxTopK];
     __shared__ int isel[kMaxTopK], ivalid[kMaxTopK];
+    __shared__ float part[kMaxGuRows * 2 * 2];   // gate/up partial sums per (row, pass)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
             mb_init(&full[s], 1);
-            mb_init(&empty[s], 8);      // one arrival per compute warp
+            mb_init(&empty[s], kWarpsC);     // one arrival per compute warp
         }
         mb_init(&idx_ready, 1);
+        mb_init(&h_ready, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -201,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     dn_rows(a, d0, d1);
     const int rows = d1 - d0;
 
-    if (warp == 8) {
+    if (warp == kWarpsC) {
         // ================= producer: bulk copies into the ring =================
         if (lane == 0) {
             if (!mb_wait(&idx_ready, 0, a.status)) return;
@@ -217,8 +308,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             for (int k = 0; gu_item(a, k, it); ++k) {
                 uint32_t s;
                 unsigned char *dst = acquire(s);
-                const int e = isel[it.i];
-                const size_t row = (size_t)e * F + it.j0;
+                const size_t row = (size_t)isel[it.i] * F + it.j0;
                 const uint32_t cb = it.n * (D / 2), sb = it.n * NG * 2;
                 mb_expect(&full[s], 2 * cb + 4 * sb);
                 bulk_g2s(dst, a.gq + row * (D / 2), cb, &full[s]);
@@ -252,29 +342,25 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     }
 
     // ================= compute warps =================
-    // router row of this CTA: load before waiting on the previous kernel
+    // this CTA's router row: requested before waiting on the previous kernel
     uint4 rw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     const bool has_row = kRoute && (int)blockIdx.x < E;
-    if (has_row) {
-        const uint16_t *wr = a.router_w + (size_t)blockIdx.x * D;
-        for (int q = 0; q < 2; ++q) {
-            const int d = (tid + q * kCompute) * 8;
-            if (d < D) rw[q] = ld_stream16(wr + d);
-        }
-    }
+    if (has_row)
+        for (int q = 0; q < 2; ++q)
+            if ((tid + q * kCompute) * 8 < D)
+                rw[q] = ld_stream16(a.router_w + (size_t)blockIdx.x * D + (tid + q * kCompute) * 8);
 
     pdl_wait();
     pdl_launch_dependents();
 
-    // ---- normalise x: each thread owns 8 consecutive elements per pass ----
+    // ---- normalise x: thread t owns elements [8(t + q*kCompute), +8), q = 0, 1 ----
     float xv[2][8];
-    float ss = 0.f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-        const int d = (tid + q * kCompute) * 8;
-        if (d < D) {
-            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.x + d));
-            *reinterpret_cast<uint4 *>(xraw + d) = v;
+        const int d8 = (tid + q * kCompute) * 8;
+        if (d8 < D) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.x + d8));
+            *reinterpret_cast<uint4 *>(xraw + d8) = v;
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -288,11 +374,14 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     }
     bar_compute();   // xraw complete before threads read each other's elements
     if (a.gain) {
-        // same reduction order as block_rms_inv (stride-256 scalar partials, warp tree, 8 warps in order)
-        for (int d = tid; d < D; d += kCompute) {
-            const float v = bf16_to_f32(xraw[d]);
-            ss = fmaf(v, v, ss);
-        }
+        // the reduction order of block_rms_inv: stride-256 scalar partials,
+        // a warp tree, then the 8 warp sums in order
+        float ss = 0.f;
+        if (tid < 256)
+            for (int d = tid; d < D; d += 256) {
+                const float v = bf16_to_f32(xraw[d]);
+                ss = fmaf(v, v, ss);
+            }
         ss = warp_sum(ss);
         if (lane == 0) red[warp] = ss;
         bar_compute();
@@ -302,38 +391,36 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         const float inv = 1.0f / sqrtf(t / (float)D + a.eps);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const int d = (tid + q * kCompute) * 8;
-            if (d < D) {
-                const uint4 gv = *reinterpret_cast<const uint4 *>(a.gain + d);
+            const int d8 = (tid + q * kCompute) * 8;
+            if (d8 < D) {
+                const uint4 gv = *reinterpret_cast<const uint4 *>(a.gain + d8);
                 const uint16_t *gg = reinterpret_cast<const uint16_t *>(&gv);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) xv[q][k] = bf16_to_f32(rms_apply(xraw[d + k], inv, gg[k]));
+                for (int k = 0; k < 8; ++k) xv[q][k] = bf16_to_f32(rms_apply(xraw[d8 + k], inv, gg[k]));
             }
         }
     }
-    // stage xn (fp32) lane-interleaved for the gate/up sweep: chunk c (32 values)
-    // = pass*64 + half*32 + l sits at float4 ((pass*2+half)*8 + k)*32 + l.
-    float part = 0.f;
+    // stage xn (fp32) lane-interleaved for the gate/up sweep: chunk
+    // c = pass*64 + half*32 + l sits at float4 ((pass*2+half)*8 + k)*32 + l.
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-        const int d = (tid + q * kCompute) * 8;
-        if (d < D) {
-            const int c = d >> 5, k0 = (d & 31) >> 2;   // chunk, first float4 within it
+        const int d8 = (tid + q * kCompute) * 8;
+        const bool own = d8 < D;
+        if (own) {
+            const int c = d8 >> 5, k0 = (d8 & 31) >> 2;
             const int pass = c >> 6, hl = (c >> 5) & 1, l = c & 31;
             float4 *dst = reinterpret_cast<float4 *>(xs) + ((pass * 2 + hl) * 8 + k0) * 32 + l;
             dst[0] = make_float4(xv[q][0], xv[q][1], xv[q][2], xv[q][3]);
             dst[32] = make_float4(xv[q][4], xv[q][5], xv[q][6], xv[q][7]);
-            float s8 = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) s8 += xv[q][k];
-            // 4 consecutive threads hold one 32-element chunk
-            s8 += __shfl_xor_sync(0xffffffffu, s8, 1);
-            s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
-            if ((tid & 3) == 0) xc[c] = s8;
         }
+        float s8 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s8 += xv[q][k];
+        s8 += __shfl_xor_sync(0xffffffffu, s8, 1);     // 4 consecutive threads = one chunk
+        s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
+        if (own && (tid & 3) == 0) xc[d8 >> 5] = s8;
     }
-    // chunks past D (D not a multiple of 2048) read as zero
-    for (int c = NC + tid; c < NCP * 64; c += kCompute) {
+    for (int c = NC + tid; c < NCP * 64; c += kCompute) {   // chunks past D read as zero
         const int pass = c >> 6, hl = (c >> 5) & 1, l = c & 31;
         for (int k = 0; k < 8; ++k)
             reinterpret_cast<float4 *>(xs)[((pass * 2 + hl) * 8 + k) * 32 + l] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -359,24 +446,30 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             bar_compute();
             if (tid == 0) {
                 float t = 0.f;
-                for (int i = 0; i < 8; ++i) t += red[i];
+                for (int i = 0; i < kWarpsC; ++i) t += red[i];
                 a.logits[blockIdx.x] = t;
             }
         }
-        grid_sync(a.bar, a.status);
+        grid_sync(a.gctr, a.status);
         float my = -INFINITY;
+        unsigned long long mykey = 0;
         if (tid < E) {
             my = __ldcg(a.logits + tid);
-            keys[tid] = order_key(my);
+            // unique key: larger logit first, equal logits keep the lower id
+            mykey = ((unsigned long long)order_key(my) << 32) | (0xFFFFFFFFu - (uint32_t)tid);
+            keys[tid] = mykey;
         }
         bar_compute();
         if (tid < E) {
-            const uint32_t k0 = keys[tid];
-            int rank = 0;
-            for (int j = 0; j < E; ++j) {
-                const uint32_t kj = keys[j];
-                rank += (kj > k0) | ((kj == k0) & (j < tid));
+            int r0 = 0, r1 = 0;
+            const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(keys);
+            for (int j = 0; j < E / 2; ++j) {
+                const ulonglong2 kk = k2[j];
+                r0 += kk.x > mykey;
+                r1 += kk.y > mykey;
             }
+            if (E & 1) r0 += keys[E - 1] > mykey;
+            const int rank = r0 + r1;
             if (rank < K) {
                 isel[rank] = tid;
                 lsel[rank] = my;
@@ -390,10 +483,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         } else {
             float pz = (tid < E) ? expf(my - m) : 0.f;
             pz = warp_sum(pz);
-            bar_compute();
             if (lane == 0) red[warp] = pz;
             bar_compute();
-            for (int i = 0; i < 8; ++i) denom += red[i];
+            for (int i = 0; i < kWarpsC; ++i) denom += red[i];
         }
         if (tid < K) {
             wsel[tid] = expf(lsel[tid] - m) / denom;
@@ -426,92 +518,94 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     bar_compute();
     if (tid == 0) mb_arrive(&idx_ready);
 
-    // ---- phase 1: gate/up rows -> h ----
+    // ---- phase 1: gate/up rows -> partial sums, the activations in registers ----
+    // Warp w takes pass pw = w % NCP (chunks pw*64 + lane and pw*64 + 32 + lane
+    // of every row, so its 64 activations stay in registers) and row slot
+    // w / NCP of each item; the NCP partial sums of a row meet in shared memory.
     uint32_t g = 0;
+    const int p0 = (int)((long long)K * F * blockIdx.x / gridDim.x);
+    const int p1 = (int)((long long)K * F * (blockIdx.x + 1) / gridDim.x);
     {
         const int NG = D / kGroup;
+        const int pw = warp % NCP, rs = warp / NCP, rstep = kWarpsC / NCP;
         const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
+        const int ca = pw * 64 + lane, cbk = ca + 32;
+        float4 xa[8], xb[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            xa[q] = xs4[((pw * 2 + 0) * 8 + q) * 32 + lane];
+            xb[q] = xs4[((pw * 2 + 1) * 8 + q) * 32 + lane];
+        }
+        const float Xa = xc[ca], Xb = xc[cbk];
         GuIt it;
         for (int k = 0; gu_item(a, k, it); ++k, ++g) {
             const uint32_t s = g % kSlots;
-            mb_wait(&full[s], (g / kSlots) & 1, a.status);
+            warp_wait(&full[s], (g / kSlots) & 1, a.status);
             const unsigned char *slot = ring + s * a.slot_bytes;
-            const uint32_t cb = it.n * (D / 2), sb = it.n * NG * 2;
+            const uint32_t cb = it.n * (D / 2);
             const uint16_t *gsr = reinterpret_cast<const uint16_t *>(slot + 2 * cb);
             const uint16_t *gbr = gsr + it.n * NG, *usr = gbr + it.n * NG, *ubr = usr + it.n * NG;
-            for (int r0 = warp; r0 < it.n; r0 += 16) {
-                const int r1 = r0 + 8;
-                const bool two = r1 < it.n;
-                float ag0 = 0.f, au0 = 0.f, ag1 = 0.f, au1 = 0.f;
-                for (int pass = 0; pass < NCP; ++pass) {
-#pragma unroll
-                    for (int hl = 0; hl < 2; ++hl) {
-                        const int c = pass * 64 + hl * 32 + lane;
-                        if (c >= NC) continue;
-                        float4 xq[8];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) xq[k] = xs4[((pass * 2 + hl) * 8 + k) * 32 + lane];
-                        const float X = xc[c];
-                        const int gi = c >> 1;
-                        {
-                            const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r0 * (D / 2) + c * 16);
-                            const uint4 cu = *reinterpret_cast<const uint4 *>(slot + cb + r0 * (D / 2) + c * 16);
-                            float2 A = make_float2(0.f, 0.f), B = make_float2(0.f, 0.f);
-                            dot8(cg.x, xq[0], xq[1], A); dot8(cg.y, xq[2], xq[3], A);
-                            dot8(cg.z, xq[4], xq[5], A); dot8(cg.w, xq[6], xq[7], A);
-                            dot8(cu.x, xq[0], xq[1], B); dot8(cu.y, xq[2], xq[3], B);
-                            dot8(cu.z, xq[4], xq[5], B); dot8(cu.w, xq[6], xq[7], B);
-                            const float s0 = bf16_to_f32(gsr[r0 * NG + gi]), b0 = bf16_to_f32(gbr[r0 * NG + gi]);
-                            const float s1 = bf16_to_f32(usr[r0 * NG + gi]), b1 = bf16_to_f32(ubr[r0 * NG + gi]);
-                            ag0 += s0 * (A.x + A.y) + (b0 - 128.f * s0) * X;
-                            au0 += s1 * (B.x + B.y) + (b1 - 128.f * s1) * X;
-                        }
-                        if (two) {
-                            const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r1 * (D / 2) + c * 16);
-                            const uint4 cu = *reinterpret_cast<const uint4 *>(slot + cb + r1 * (D / 2) + c * 16);
-                            float2 A = make_float2(0.f, 0.f), B = make_float2(0.f, 0.f);
-                            dot8(cg.x, xq[0], xq[1], A); dot8(cg.y, xq[2], xq[3], A);
-                            dot8(cg.z, xq[4], xq[5], A); dot8(cg.w, xq[6], xq[7], A);
-                            dot8(cu.x, xq[0], xq[1], B); dot8(cu.y, xq[2], xq[3], B);
-                            dot8(cu.z, xq[4], xq[5], B); dot8(cu.w, xq[6], xq[7], B);
-                            const float s0 = bf16_to_f32(gsr[r1 * NG + gi]), b0 = bf16_to_f32(gbr[r1 * NG + gi]);
-                            const float s1 = bf16_to_f32(usr[r1 * NG + gi]), b1 = bf16_to_f32(ubr[r1 * NG + gi]);
-                            ag1 += s0 * (A.x + A.y) + (b0 - 128.f * s0) * X;
-                            au1 += s1 * (B.x + B.y) + (b1 - 128.f * s1) * X;
-                        }
-                    }
+            for (int r = rs; r < it.n; r += rstep) {
+                float ag = 0.f, au = 0.f;
+                if (ca < NC) {
+                    const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r * (D / 2) + ca * 16);
+                    const uint4 cu = *reinterpret_cast<const uint4 *>(slot + cb + r * (D / 2) + ca * 16);
+                    const float A = dot32(cg, xa), B = dot32(cu, xa);
+                    const int gi = r * NG + (ca >> 1);
+                    const float s0 = bf16_to_f32(gsr[gi]), b0 = bf16_to_f32(gbr[gi]);
+                    const float s1 = bf16_to_f32(usr[gi]), b1 = bf16_to_f32(ubr[gi]);
+                    ag = s0 * A + (b0 - 128.f * s0) * Xa;
+                    au = s1 * B + (b1 - 128.f * s1) * Xa;
                 }
-                ag0 = warp_sum(ag0); au0 = warp_sum(au0);
-                ag1 = warp_sum(ag1); au1 = warp_sum(au1);
+                if (cbk < NC) {
+                    const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r * (D / 2) + cbk * 16);
+                    const uint4 cu = *reinterpret_cast<const uint4 *>(slot + cb + r * (D / 2) + cbk * 16);
+                    const float A = dot32(cg, xb), B = dot32(cu, xb);
+                    const int gi = r * NG + (cbk >> 1);
+                    const float s0 = bf16_to_f32(gsr[gi]), b0 = bf16_to_f32(gbr[gi]);
+                    const float s1 = bf16_to_f32(usr[gi]), b1 = bf16_to_f32(ubr[gi]);
+                    ag += s0 * A + (b0 - 128.f * s0) * Xb;
+                    au += s1 * B + (b1 - 128.f * s1) * Xb;
+                }
+                ag = warp_sum(ag);
+                au = warp_sum(au);
                 if (lane == 0) {
-                    const bool ok = ivalid[it.i];
-                    a.h[(size_t)it.i * F + it.j0 + r0] = ok ? silu_mul(ag0, au0) : 0.f;
-                    if (two) a.h[(size_t)it.i * F + it.j0 + r1] = ok ? silu_mul(ag1, au1) : 0.f;
+                    const int t = it.i * F + it.j0 + r - p0;     // row pair index within this CTA
+                    part[(t * NCP + pw) * 2] = ag;
+                    part[(t * NCP + pw) * 2 + 1] = au;
                 }
             }
             __syncwarp();
             if (lane == 0) mb_arrive(&empty[s]);
         }
     }
-
-    // ---- barrier 2: all of h written ----
-    __threadfence();
-    grid_sync(a.bar, a.status);
-
-    // ---- stage h (fp32, lane-interleaved for 8-lane subgroups) and chunk sums ----
-    for (int q = tid; q < K * MC * 64; q += kCompute) {
-        const int i = q / (MC * 64), rem = q - i * MC * 64;
-        const int m = rem / 64, k = (rem / 8) & 7, cs = rem & 7;
-        const int c = cs + 8 * m;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < FC) v = __ldcg(reinterpret_cast<const float4 *>(a.h + (size_t)i * F + c * 32 + k * 4));
-        reinterpret_cast<float4 *>(hs)[q] = v;
-    }
     bar_compute();
+    // combine the passes of each row (fixed order) and store h where the down phase reads it
+    for (int t = tid; t < p1 - p0; t += kCompute) {
+        float ag = 0.f, au = 0.f;
+        for (int q = 0; q < NCP; ++q) {
+            ag += part[(t * NCP + q) * 2];
+            au += part[(t * NCP + q) * 2 + 1];
+        }
+        const int pp = p0 + t, i = pp / F, j = pp - i * F;
+        a.h[h_pos(i, j, MC)] = ivalid[i] ? silu_mul(ag, au) : 0.f;
+    }
+
+    // ---- barrier: all of h written; then one bulk copy brings it in ----
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // h stores -> later bulk reads
+    __threadfence();
+    grid_sync(a.gctr, a.status);
+    const uint32_t hbytes = (uint32_t)(K * MC * 256 * 4);
+    if (tid == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mb_expect(&h_ready, hbytes);
+        bulk_g2s(hs, a.h, hbytes, &h_ready);
+    }
+    warp_wait(&h_ready, 0, a.status);
+    // chunk sums of h, once per CTA (each is reused by every down row of the CTA)
     for (int q = tid; q < K * MC * 8; q += kCompute) {
         const int i = q / (MC * 8), c = q - i * MC * 8;
-        const int m = c / 8, cs = c & 7;
-        const float4 *hp = reinterpret_cast<const float4 *>(hs) + ((i * MC + m) * 8) * 8 + cs;
+        const float4 *hp = reinterpret_cast<const float4 *>(hs) + ((i * MC + (c >> 3)) * 8) * 8 + (c & 7);
         float sacc = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -522,44 +616,18 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     }
     bar_compute();
 
-    // ---- phase 2: down rows of this CTA (8-lane subgroup per (expert, row)) ----
-    const int s8 = lane & 7, S = warp * 4 + (lane >> 3);
+    // ---- phase 2: down rows of this CTA ----
     const float4 *hs4 = reinterpret_cast<const float4 *>(hs);
-    const int FG = F / kGroup;
     if (rows > 0) {
         for (int i0 = 0; i0 < K; i0 += a.e_dn, ++g) {
             const int ne = min(a.e_dn, K - i0);
             const uint32_t s = g % kSlots;
-            mb_wait(&full[s], (g / kSlots) & 1, a.status);
+            warp_wait(&full[s], (g / kSlots) & 1, a.status);
             const unsigned char *slot = ring + s * a.slot_bytes;
-            const uint32_t cb = rows * (F / 2), sb = rows * FG * 2;
-            // warp-uniform trip count: every lane reaches the shuffles below
-            for (int base = warp * 4; base < ne * rows; base += 32) {
-                const int q = base + (S - warp * 4);
-                const bool live = q < ne * rows;
-                const int qi = live ? q / rows : 0, r = live ? q - qi * rows : 0, i = i0 + qi;
-                const unsigned char *rp = slot + qi * cb + r * (F / 2);
-                const uint16_t *sr = reinterpret_cast<const uint16_t *>(slot + ne * cb + qi * 2 * sb) + r * FG;
-                const uint16_t *br = sr + rows * FG;
-                float acc = 0.f;
-                for (int m = 0; m < MC && live; ++m) {
-                    const int c = s8 + 8 * m;
-                    if (c >= FC) break;
-                    const uint4 cv = *reinterpret_cast<const uint4 *>(rp + c * 16);
-                    const float4 *hv = hs4 + ((i * MC + m) * 8) * 8 + s8;
-                    float2 A = make_float2(0.f, 0.f);
-                    dot8(cv.x, hv[0], hv[8], A);
-                    dot8(cv.y, hv[16], hv[24], A);
-                    dot8(cv.z, hv[32], hv[40], A);
-                    dot8(cv.w, hv[48], hv[56], A);
-                    const float sc = bf16_to_f32(sr[c >> 1]), bi = bf16_to_f32(br[c >> 1]);
-                    acc += sc * (A.x + A.y) + (bi - 128.f * sc) * hc[(i * MC + m) * 8 + s8];
-                }
-                acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                if (live && s8 == 0) os[i * a.rows_max + r] = acc;
-            }
+            if (a.dn_sg == 8)
+                down_item<8, 2>(slot, i0, ne, rows, F, MC, hs4, hc, os, a.rows_max);
+            else
+                down_item<16, 1>(slot, i0, ne, rows, F, MC, hs4, hc, os, a.rows_max);
             __syncwarp();
             if (lane == 0) mb_arrive(&empty[s]);
         }
@@ -583,14 +651,13 @@ bool fused_plan(FusedArgs &a, int num_sms) {
     const int D = a.D, F = a.F, K = a.K;
     if (D % 512 || F % 128 || D > 4096 || K > kMaxTopK) return false;
     // bulk copies need 16-byte aligned sources
-    const void *ptrs[] = {a.gq, a.uq, a.dq, a.gs, a.gb, a.us, a.ub, a.ds, a.db, a.x};
+    const void *ptrs[] = {a.gq, a.uq, a.dq, a.gs, a.gb, a.us, a.ub, a.ds, a.db, a.x, a.h};
     for (const void *q : ptrs)
         if (reinterpret_cast<uintptr_t>(q) % 16) return false;
     if (a.gain && reinterpret_cast<uintptr_t>(a.gain) % 16) return false;
     a.grid = num_sms;
     if (a.E > a.grid) return false;
     const int NG = D / kGroup, FG = F / kGroup;
-    // down rows: units of dn_gran rows whose scale block starts 16-byte aligned
     int gran = 1;
     while ((gran * (F / 32)) % 16) ++gran;
     a.dn_gran = gran;
@@ -598,24 +665,36 @@ bool fused_plan(FusedArgs &a, int num_sms) {
     a.rows_max = ((units + a.grid - 1) / a.grid) * gran;
     const int row_pair_bytes = 2 * (D / 2 + NG * 2 * 2);
     const int dn_bytes_1 = a.rows_max * (F / 2 + FG * 2 * 2);
-    // slots: gate/up items of r_gu rows, down items of e_dn experts
-    const int target = D >= 4096 ? 36 * 1024 : 20 * 1024;
-    a.r_gu = target / row_pair_bytes;
-    if (a.r_gu < 1) a.r_gu = 1;
-    if (a.r_gu > 16) a.r_gu = 16;
-    a.e_dn = (a.r_gu * row_pair_bytes) / dn_bytes_1;
-    if (a.e_dn < 1) a.e_dn = 1;
+    // gate/up: one row pair per (group of NCP warps) per item
+    const int NCPh = (D / 32 + 63) / 64;
+    a.r_gu = kWarpsC / NCPh;
+    while (a.r_gu > 1 && a.r_gu * row_pair_bytes > kSlotMax) --a.r_gu;
+    // down: as many experts per item as fit in a slot
+    a.e_dn = kSlotMax / dn_bytes_1;
     if (a.e_dn > K) a.e_dn = K;
+    if (a.e_dn < 1) return false;
+    // subgroup width: 8 lanes x 2 rows, or 16 lanes x 1 row -- fewer rounds x chunks wins
+    {
+        const int FCh = F / 32;
+        const int units8 = a.e_dn * ((a.rows_max + 1) / 2), units16 = a.e_dn * a.rows_max;
+        const int cost8 = ((units8 + kWarpsC * 4 - 1) / (kWarpsC * 4)) * ((FCh + 7) / 8) * 2;
+        const int cost16 = ((units16 + kWarpsC * 2 - 1) / (kWarpsC * 2)) * ((FCh + 15) / 16);
+        a.dn_sg = cost16 < cost8 ? 16 : 8;
+    }
     a.slot_bytes = max(a.r_gu * row_pair_bytes, a.e_dn * dn_bytes_1);
     a.slot_bytes = (a.slot_bytes + 127) / 128 * 128;
     a.ring_bytes = kSlots * a.slot_bytes;
     const int NCP = (D / 32 + 63) / 64, MC = (F / 32 + 7) / 8;
     const int xs_bytes = (NCP * 2048 + NCP * 64) * 4;
     const int hs_bytes = (K * MC * 256 + K * MC * 8) * 4;
+    if ((K * F + a.grid - 1) / a.grid > kMaxGuRows || D / 32 > 128) return false;
     a.union_bytes = (max(xs_bytes, hs_bytes) + 127) / 128 * 128;
     a.smem_bytes = a.ring_bytes + a.union_bytes + D * 2 + K * a.rows_max * 4;
-    return a.smem_bytes <= 200 * 1024;
+    return a.smem_bytes <= 210 * 1024;
 }
+
+// Floats of h scratch the fused kernel needs (its padded down-phase layout).
+size_t fused_h_floats(int F, int K) { return (size_t)K * ((F / 32 + 7) / 8) * 256; }
 
 cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route) {
     static int attr[2] = {0, 0};

@@ -88,7 +88,7 @@ struct FusedArgs {
     const uint16_t *gs, *gb, *us, *ub, *ds, *db;
     float *logits;              // [E] scratch
     float *h;                   // [K][F] scratch
-    uint32_t *bar;              // grid barrier {count, generation}
+    unsigned long long *gctr;   // grid barrier arrival counter (only grows)
     int32_t *status;
     int32_t *idx_out;           // [K] (route variant)
     float *w_out;               // [K]
@@ -96,9 +96,10 @@ struct FusedArgs {
     const float *w_in;          // [K]
     float *expert_out;          // [K][D] or NULL
     // plan (fused_plan)
-    int grid, r_gu, e_dn, dn_gran, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
+    int grid, r_gu, e_dn, dn_gran, dn_sg, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
 };
 bool fused_plan(FusedArgs &a, int num_sms);
+size_t fused_h_floats(int F, int K);
 cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route);
 
 struct PrefillArgs {

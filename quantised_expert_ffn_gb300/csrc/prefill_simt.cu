@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(kThreads) k_prefill_combine(PrefillArgs a) {
         wt[threadIdx.x] = a.w[t * a.K + threadIdx.x];
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < a.D; d += kThreads) {
+    // CTA (t, blockIdx.y) covers elements [1024*by, 1024*by + 1024) of token t
+    const int dend = min(a.D, (int)(blockIdx.y + 1) * 1024);
+    for (int d = blockIdx.y * 1024 + threadIdx.x; d < dend; d += kThreads) {
         float y = bf16_to_f32(a.x[(size_t)t * a.D + d]);
         for (int i = 0; i < a.K; ++i)
             if (slot[i] >= 0) y = fmaf(wt[i], __ldcg(a.obuf + (size_t)slot[i] * a.D + d), y);
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) k_prefill_combine(PrefillArgs a) {
 }
 
 cudaError_t launch_prefill_combine(const PrefillArgs &a, cudaStream_t s, bool pdl) {
-    return launch_kernel(k_prefill_combine, dim3(a.T), dim3(kThreads), 0, s, pdl, a);
+    return launch_kernel(k_prefill_combine, dim3(a.T, (a.D + 1023) / 1024), dim3(kThreads), 0, s, pdl, a);
 }
 
 cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float *h32,
@@ -174,7 +176,7 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float 
     if (err != cudaSuccess) return err;
     err = launch_kernel(k_prefill_down_simt, dim3((a.D + 7) / 8, a.E), dim3(kThreads), 0, s, pdl, sa);
     if (err != cudaSuccess) return err;
-    return launch_kernel(k_prefill_combine, dim3(a.T), dim3(kThreads), 0, s, pdl, a);
+    return launch_prefill_combine(a, s, pdl);
 }
 
 }  // namespace smoe

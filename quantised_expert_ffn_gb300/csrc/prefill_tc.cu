@@ -111,8 +111,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile
     if (mbar_try(b, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try(b, parity)) return true;
+        if (mbar_try_suspend(smem_u32(b), parity, kSuspendHintNs)) return true;
         if (*abort_flag) return false;
         if (global_ns() - t0 > kWaitLimitNs) break;
     }

@@ -29,7 +29,8 @@ SMOE_ERR_DEVICE = -6
 class SmoeError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {smoe_status_string(status)} ({status})")
+        extra = f" [{smoe_last_cuda_error()}]" if status == SMOE_ERR_CUDA else ""
+        super().__init__(f"{where}: {smoe_status_string(status)} ({status}){extra}")
 
 
 class smoe_layer(ctypes.Structure):
@@ -72,6 +73,7 @@ def _load():
         "smoe_moe_prefill_chunk": (I, [LP, P, I, P, P, P, P, Z, P]),
         "smoe_status_string": (ctypes.c_char_p, [I]),
         "smoe_moe_decode_noalloc": (I, [LP, P, P, P, P, P]),
+        "smoe_last_cuda_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -83,7 +85,8 @@ def _load():
 _lib = _load()
 EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_status",
             "smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_ffn_decode",
-            "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc")
+            "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc",
+            "smoe_last_cuda_error")
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -98,6 +101,10 @@ def _stream(stream=None):
 def _check(status: int, where: str):
     if status != SMOE_OK:
         raise SmoeError(status, where)
+
+
+def smoe_last_cuda_error() -> str:
+    return _lib.smoe_last_cuda_error().decode()
 
 
 def smoe_status_string(status: int) -> str:
