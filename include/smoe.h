@@ -189,10 +189,10 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
 
 /* Decode without a workspace.  The pages have no counterpart of this call:
  * it exists for callers that cannot allocate device memory when they run a
- * layer -- code inside a CUDA graph capture (an allocation cannot be
- * captured), real-time loops whose latency budget rules out the device-wide
- * synchronisation an allocation may cause, and plug-ins whose host program
- * owns all device memory through its own pool.
+ * layer -- real-time loops whose latency budget rules out the device-wide
+ * synchronisation an allocation may cause, services that reserve all their
+ * device memory at start-up and must not grow afterwards, and plug-ins whose
+ * host program owns all device memory through its own pool.
  * Computes exactly what smoe_moe_decode computes (same kernels); the scratch
  * lives in a fixed device array of the library, SMOE_DECODE_NOALLOC_MAX_BYTES
  * bytes, that every GPU which loads the library holds until the process

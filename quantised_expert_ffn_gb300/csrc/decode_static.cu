@@ -3,9 +3,9 @@
 // library instead of a caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the moment they need to run
-// a layer: code that runs inside a CUDA graph capture (cudaMalloc is not a
-// capturable operation), real-time serving loops whose latency budget rules
-// out the device-wide synchronisation an allocation can cause, and plug-ins
+// a layer: real-time serving loops whose latency budget rules out the
+// device-wide synchronisation an allocation can cause, services that reserve
+// all their device memory at start-up and must not grow later, and plug-ins
 // loaded into a host program that owns every byte of device memory through
 // its own pool.  This entry point lets them decode without a workspace: the
 // scratch (status word, route and barrier counters, logits, expert ids and
@@ -22,7 +22,7 @@ constexpr size_t kStaticScratchBytes = 512 * 1024;   // largest layer this entry
 constexpr size_t kClearBytes = 1024;                  // status word, route tickets, grid barrier
 constexpr int kMaxDevices = 64;
 
-__device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 // Device address of g_decode_scratch for each device, looked up once with that
 // device current.  In host code the array's name is only a host-side stand-in,

@@ -195,7 +195,7 @@ SMOE_DECODE_NOALLOC_MAX_BYTES = 512 * 1024
 
 def smoe_moe_decode_noalloc(layer: Layer, x, y, idx_out=None, w_out=None, stream=None):
     """Decode one token with the library's fixed device scratch instead of a
-    workspace (for callers that cannot allocate device memory, e.g. inside a
-    graph capture); see include/smoe.h."""
+    workspace (for callers that cannot allocate device memory, e.g. latency-bound
+    serving loops or plug-ins whose host owns the device memory); see include/smoe.h."""
     _check(_lib.smoe_moe_decode_noalloc(layer.ref, _p(x), _p(y), _p(idx_out), _p(w_out),
                                         _stream(stream)), "smoe_moe_decode_noalloc")

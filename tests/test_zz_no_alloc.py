@@ -1,6 +1,6 @@
 """smoe_moe_decode_noalloc: decode without a workspace, for callers that cannot
-allocate device memory (inside a graph capture, latency-bound serving loops,
-plug-ins whose host owns the device memory).  Its output must match the
+allocate device memory (latency-bound serving loops, services whose device
+memory is fixed at start-up, plug-ins whose host owns the device memory).  Its output must match the
 workspace entry point's, call after call: the fixed scratch keeps the previous
 call's contents, so two calls in a row are checked.  This file is collected
 last so that a failure here comes after every other test has run."""
