@@ -151,104 +151,31 @@ __device__ __forceinline__ float dot32(uint4 c, const float4 (&x)[8]) {
 
 // ---------------------------------------------------------------- work lists
 
-// Gate/up: CTA c owns row pairs [P*c/G, P*(c+1)/G) of the K*F (slot, row)
-// pairs; an item is up to r_gu consecutive rows of one expert slot.
-struct GuIt {
-    int i, j0, n;   // expert slot, first row, rows
-};
-__device__ __forceinline__ bool gu_item(const FusedArgs &a, int idx, GuIt &it) {
-    const long long P = (long long)a.K * a.F;
-    int p = (int)(P * blockIdx.x / gridDim.x);
-    const int p1 = (int)(P * (blockIdx.x + 1) / gridDim.x);
-    for (int k = 0; p < p1; ++k) {
-        const int i = p / a.F, j = p - i * a.F;
-        const int n = min(a.r_gu, min(p1 - p, a.F - j));
-        if (k == idx) {
-            it = {i, j, n};
-            return true;
-        }
-        p += n;
-    }
-    return false;
+// Gate/up: CTA c owns row pairs [P*c/G, P*(c+1)/G) of the P = K*F (slot, row)
+// pairs; an item is up to r_gu consecutive rows of one expert slot.  All
+// products stay below 2^31 (K*F <= 16384, G <= 256).
+__device__ __forceinline__ void gu_range(const FusedArgs &a, int &p0, int &p1) {
+    const int P = a.K * a.F;
+    p0 = P * (int)blockIdx.x / (int)gridDim.x;
+    p1 = P * ((int)blockIdx.x + 1) / (int)gridDim.x;
 }
 
 // Down: CTA c owns output rows [d0, d1), multiples of a.dn_gran rows (so each
-// row block's scale block starts 16-byte aligned); an item is up to a.e_dn
-// consecutive expert slots of those rows.
+// row block's scale block starts 16-byte aligned); an item is a block of up to
+// a.dn_nr of those rows (a multiple of dn_gran) for all K expert slots.
 __device__ __forceinline__ void dn_rows(const FusedArgs &a, int &d0, int &d1) {
     const int units = a.D / a.dn_gran;
-    d0 = (int)((long long)units * blockIdx.x / gridDim.x) * a.dn_gran;
-    d1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x) * a.dn_gran;
+    d0 = units * (int)blockIdx.x / (int)gridDim.x * a.dn_gran;
+    d1 = units * ((int)blockIdx.x + 1) / (int)gridDim.x * a.dn_gran;
 }
 
-// Position of h[i][f] in the down phase's layout: chunk c = f/32 is handled by
-// lane s8 = c%8 of a subgroup in round m = c/8; float4 k = (f%32)/4 of the
-// chunk sits at ((i*MC + m)*8 + k)*8 + s8 (conflict-free 16-byte reads).
+// Position of h[i][f] in the down phase's layout: chunk c = f/32 of slot i is
+// read by the thread that owns (i, c); float4 k = (f%32)/4 of the chunk sits at
+// ((i*MC + c/8)*8 + k)*8 + c%8, so the 8 threads of a phase that own
+// consecutive chunks read 128 consecutive bytes (no bank conflicts).
 __device__ __forceinline__ int h_pos(int i, int f, int MC) {
     const int c = f >> 5, k = (f & 31) >> 2;
     return ((((i * MC + (c >> 3)) * 8 + k) * 8 + (c & 7)) << 2) + (f & 3);
-}
-
-// ---------------------------------------------------------------- down phase
-
-// One down item (experts i0..i0+ne-1, this CTA's `rows` rows) from ring slot
-// `slot`: an SG-lane subgroup takes RU rows of one expert; lane l handles chunks
-// l, l+SG, l+2SG, ... of each row, so one 32-value h load serves RU rows.  The
-// sums of the item's (expert, row) pairs go to os[i][r].
-template <int SG, int RU>
-__device__ __forceinline__ void down_item(const unsigned char *slot, int i0, int ne, int rows, int F, int MC,
-                                          const float4 *hs4, const float *hc, float *os, int rows_max) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int l = lane % SG, sub = lane / SG;
-    constexpr int kSubPerWarp = 32 / SG;
-    const int FC = F / 32, FG = F / kGroup;
-    const uint32_t cb = rows * (F / 2), sb = rows * FG * 2;
-    const int RP = (rows + RU - 1) / RU;
-    const int units = ne * RP;
-    // warp-uniform trip count: every lane reaches the shuffles below
-    for (int base = warp * kSubPerWarp; base < units; base += kWarpsC * kSubPerWarp) {
-        const int q = base + sub;
-        const bool live = q < units;
-        const int qi = live ? q / RP : 0, rp = live ? q - qi * RP : 0, i = i0 + qi;
-        float acc[RU];
-        const unsigned char *rowp[RU];
-        const uint16_t *srp[RU], *brp[RU];
-#pragma unroll
-        for (int u = 0; u < RU; ++u) {
-            acc[u] = 0.f;
-            const int r = min(rp * RU + u, rows - 1);            // a missing last row repeats a real one
-            rowp[u] = slot + qi * cb + r * (F / 2);
-            srp[u] = reinterpret_cast<const uint16_t *>(slot + ne * cb + qi * 2 * sb) + r * FG;
-            brp[u] = srp[u] + rows * FG;
-        }
-        if (live) {
-            for (int c = l; c < FC; c += SG) {
-                const float4 *hv = hs4 + ((i * MC + (c >> 3)) * 8) * 8 + (c & 7);
-                float4 hq[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) hq[k] = hv[k * 8];
-                const float H = hc[(i * MC + (c >> 3)) * 8 + (c & 7)];
-                uint4 cv[RU];
-#pragma unroll
-                for (int u = 0; u < RU; ++u) cv[u] = *reinterpret_cast<const uint4 *>(rowp[u] + c * 16);
-#pragma unroll
-                for (int u = 0; u < RU; ++u) {
-                    const float A = dot32(cv[u], hq);
-                    const float sc = bf16_to_f32(srp[u][c >> 1]), bi = bf16_to_f32(brp[u][c >> 1]);
-                    acc[u] += sc * A + (bi - 128.f * sc) * H;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < RU; ++u)
-#pragma unroll
-            for (int o = SG / 2; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
-        if (live && l == 0) {
-#pragma unroll
-            for (int u = 0; u < RU; ++u)
-                if (rp * RU + u < rows) os[i * rows_max + rp * RU + u] = acc[u];
-        }
-    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -259,22 +186,25 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     const int D = a.D, F = a.F, K = a.K, E = a.E;
     const int NC = D / 32;                       // 32-code chunks of a gate/up row
     const int NCP = (NC + 63) / 64;              // passes of 64 chunks (2 per lane)
-    const int FC = F / 32;                       // chunks of a down row
-    const int MC = (FC + 7) / 8;                 // chunk rounds of an 8-lane subgroup
+    const int FC = F / 32;                       // 32-code chunks of a down row
+    const int FG = F / kGroup;
+    const int MC = (FC + 7) / 8;                 // blocks of 8 chunks in the h layout
+    const int P = K * FC;                        // (slot, chunk) pairs of the down phase
     unsigned char *ring = sm;
-    float *u_region = reinterpret_cast<float *>(sm + a.ring_bytes);       // xs+xc | hs
+    float *u_region = reinterpret_cast<float *>(sm + a.ring_bytes);       // xs+xc | hs | red
     float *xs = u_region;                        // NCP*64*8 float4
     float *xc = xs + NCP * 2048;                 // NCP*64 chunk sums
-    float *hs = u_region;                        // K*MC*256 floats
-    float *hc = hs + K * MC * 256;               // K*MC*8 chunk sums of h
+    float *hs = u_region;                        // K*MC*256 floats (h, down-phase layout)
+    float *red = u_region;                       // [rows][P] down partial sums (after h is in registers)
     uint16_t *xraw = reinterpret_cast<uint16_t *>(sm + a.ring_bytes + a.union_bytes);   // [D]
     float *os = reinterpret_cast<float *>(xraw + D);                                 // [K][rows_max]
     __shared__ uint64_t full[kSlots], empty[kSlots], idx_ready, h_ready;
-    __shared__ float red[kWarpsC];
+    __shared__ float red14[kWarpsC];
     __shared__ __align__(16) unsigned long long keys[kMaxExperts];
     __shared__ float lsel[kMaxTopK], wsel[kMaxTopK];
     __shared__ int isel[kMaxTopK], ivalid[kMaxTopK];
     __shared__ float part[kMaxGuRows * 2 * 2];   // gate/up partial sums per (row, pass)
+    __shared__ int pcnt[kMaxGuRows];             // passes of a row done
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) {
@@ -286,72 +216,99 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         mb_init(&h_ready, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (tid < kMaxGuRows) pcnt[tid] = 0;
     __syncthreads();
 
-    int d0, d1;
+    int d0, d1, p0, p1;
     dn_rows(a, d0, d1);
+    gu_range(a, p0, p1);
     const int rows = d1 - d0;
 
     if (warp == kWarpsC) {
         // ================= producer: bulk copies into the ring =================
-        if (lane == 0) {
-            if (!mb_wait(&idx_ready, 0, a.status)) return;
-            uint32_t g = 0;
-            auto acquire = [&](uint32_t &s) -> unsigned char * {
-                s = g % kSlots;
+        // Lane 0 waits for a free slot and posts its byte count; then one lane
+        // per copy issues the copies of the item together.
+        int ok = 1;
+        if (lane == 0) ok = mb_wait(&idx_ready, 0, a.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        mb_try(&idx_ready, 0);                 // each lane observes the ids
+        const int NG = D / kGroup;
+        uint32_t g = 0;
+        for (int p = p0; p < p1; ++g) {
+            const int i = p / F, j0 = p - i * F, n = min(a.r_gu, min(p1 - p, F - j0));
+            const uint32_t s = g % kSlots;
+            unsigned char *dst = ring + s * a.slot_bytes;
+            const uint32_t cb = n * (D / 2), sb = n * NG * 2;
+            if (lane == 0) {
                 mb_wait(&empty[s], ((g / kSlots) & 1) ^ 1, a.status);
-                ++g;
-                return ring + s * a.slot_bytes;
-            };
-            const int NG = D / kGroup;
-            GuIt it;
-            for (int k = 0; gu_item(a, k, it); ++k) {
-                uint32_t s;
-                unsigned char *dst = acquire(s);
-                const size_t row = (size_t)isel[it.i] * F + it.j0;
-                const uint32_t cb = it.n * (D / 2), sb = it.n * NG * 2;
                 mb_expect(&full[s], 2 * cb + 4 * sb);
-                bulk_g2s(dst, a.gq + row * (D / 2), cb, &full[s]);
-                bulk_g2s(dst + cb, a.uq + row * (D / 2), cb, &full[s]);
-                bulk_g2s(dst + 2 * cb, a.gs + row * NG, sb, &full[s]);
-                bulk_g2s(dst + 2 * cb + sb, a.gb + row * NG, sb, &full[s]);
-                bulk_g2s(dst + 2 * cb + 2 * sb, a.us + row * NG, sb, &full[s]);
-                bulk_g2s(dst + 2 * cb + 3 * sb, a.ub + row * NG, sb, &full[s]);
             }
-            if (rows > 0) {
-                const int FG = F / kGroup;
-                for (int i0 = 0; i0 < K; i0 += a.e_dn) {
-                    const int ne = min(a.e_dn, K - i0);
-                    uint32_t s;
-                    unsigned char *dst = acquire(s);
-                    const uint32_t cb = rows * (F / 2), sb = rows * FG * 2;
-                    mb_expect(&full[s], ne * (cb + 2 * sb));
-                    for (int q = 0; q < ne; ++q) {
-                        const size_t row = (size_t)isel[i0 + q] * D + d0;
-                        bulk_g2s(dst + q * cb, a.dq + row * (F / 2), cb, &full[s]);
-                        bulk_g2s(dst + ne * cb + q * 2 * sb, a.ds + row * FG, sb, &full[s]);
-                        bulk_g2s(dst + ne * cb + q * 2 * sb + sb, a.db + row * FG, sb, &full[s]);
-                    }
-                }
+            __syncwarp();
+            mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
+            const size_t row = (size_t)isel[i] * F + j0;
+            if (lane < 2) {
+                bulk_g2s(dst + lane * cb, (lane ? a.uq : a.gq) + row * (D / 2), cb, &full[s]);
+            } else if (lane < 6) {
+                const uint16_t *src = lane == 2 ? a.gs : lane == 3 ? a.gb : lane == 4 ? a.us : a.ub;
+                bulk_g2s(dst + 2 * cb + (lane - 2) * sb, src + row * NG, sb, &full[s]);
             }
-            // every copy issued has landed before the CTA may exit
+            p += n;
+        }
+        for (int r0 = 0; r0 < rows; r0 += a.dn_nr, ++g) {
+            const int nr = min(a.dn_nr, rows - r0);
+            const uint32_t s = g % kSlots;
+            unsigned char *dst = ring + s * a.slot_bytes;
+            const uint32_t cb = nr * (F / 2), sb = nr * FG * 2;
+            if (lane == 0) {
+                mb_wait(&empty[s], ((g / kSlots) & 1) ^ 1, a.status);
+                mb_expect(&full[s], K * (cb + 2 * sb));
+            }
+            __syncwarp();
+            mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
+            for (int q = lane; q < 3 * K; q += 32) {
+                const int i = q % K, kind = q / K;
+                const size_t row = (size_t)isel[i] * D + d0 + r0;
+                if (kind == 0)
+                    bulk_g2s(dst + i * cb, a.dq + row * (F / 2), cb, &full[s]);
+                else
+                    bulk_g2s(dst + K * cb + ((kind - 1) * K + i) * sb, (kind == 1 ? a.ds : a.db) + row * FG, sb,
+                             &full[s]);
+            }
+        }
+        // every copy issued has landed before the CTA may exit
+        if (lane == 0)
             for (uint32_t k = (g > (uint32_t)kSlots ? g - kSlots : 0); k < g; ++k)
                 mb_wait(&full[k % kSlots], (k / kSlots) & 1, a.status);
-        }
+        __syncwarp();
         return;
     }
 
     // ================= compute warps =================
-    // this CTA's router row: requested before waiting on the previous kernel
+    // Inputs that do not depend on the previous kernel are requested before
+    // waiting for it: this CTA's router row and the RMSNorm gain.
     uint4 rw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    uint4 gv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     const bool has_row = kRoute && (int)blockIdx.x < E;
-    if (has_row)
-        for (int q = 0; q < 2; ++q)
-            if ((tid + q * kCompute) * 8 < D)
-                rw[q] = ld_stream16(a.router_w + (size_t)blockIdx.x * D + (tid + q * kCompute) * 8);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int d8 = (tid + q * kCompute) * 8;
+        if (d8 < D) {
+            if (has_row) rw[q] = ld_stream16(a.router_w + (size_t)blockIdx.x * D + d8);
+            if (a.gain) gv[q] = *reinterpret_cast<const uint4 *>(a.gain + d8);
+        }
+    }
 
     pdl_wait();
     pdl_launch_dependents();
+
+    // ids and weights given by the caller (FFN-only variant): requested now,
+    // consumed after the normalisation
+    int e_in = -1;
+    float w_in = 0.f;
+    if (!kRoute && tid < K) {
+        e_in = __ldcg(a.idx_in + tid);
+        w_in = __ldcg(a.w_in + tid);
+    }
 
     // ---- normalise x: thread t owns elements [8(t + q*kCompute), +8), q = 0, 1 ----
     float xv[2][8];
@@ -383,18 +340,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 ss = fmaf(v, v, ss);
             }
         ss = warp_sum(ss);
-        if (lane == 0) red[warp] = ss;
+        if (lane == 0) red14[warp] = ss;
         bar_compute();
         float t = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t += red[i];
+        for (int i = 0; i < 8; ++i) t += red14[i];
         const float inv = 1.0f / sqrtf(t / (float)D + a.eps);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int d8 = (tid + q * kCompute) * 8;
             if (d8 < D) {
-                const uint4 gv = *reinterpret_cast<const uint4 *>(a.gain + d8);
-                const uint16_t *gg = reinterpret_cast<const uint16_t *>(&gv);
+                const uint16_t *gg = reinterpret_cast<const uint16_t *>(&gv[q]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) xv[q][k] = bf16_to_f32(rms_apply(xraw[d8 + k], inv, gg[k]));
             }
@@ -442,11 +398,11 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             }
             acc = warp_sum(acc);
             bar_compute();
-            if (lane == 0) red[warp] = acc;
+            if (lane == 0) red14[warp] = acc;
             bar_compute();
             if (tid == 0) {
                 float t = 0.f;
-                for (int i = 0; i < kWarpsC; ++i) t += red[i];
+                for (int i = 0; i < kWarpsC; ++i) t += red14[i];
                 a.logits[blockIdx.x] = t;
             }
         }
@@ -483,9 +439,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         } else {
             float pz = (tid < E) ? expf(my - m) : 0.f;
             pz = warp_sum(pz);
-            if (lane == 0) red[warp] = pz;
+            if (lane == 0) red14[warp] = pz;
             bar_compute();
-            for (int i = 0; i < kWarpsC; ++i) denom += red[i];
+            for (int i = 0; i < kWarpsC; ++i) denom += red14[i];
         }
         if (tid < K) {
             wsel[tid] = expf(lsel[tid] - m) / denom;
@@ -496,13 +452,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         }
     } else {
         if (tid < K) {
-            int e = a.idx_in[tid];
-            if (e < 0 || e >= E) {
+            if (e_in < 0 || e_in >= E) {
                 set_status(a.status, SMOE_ERR_DEVICE);
-                e = -1;
+                e_in = -1;
             }
-            isel[tid] = e;
-            wsel[tid] = a.w_in[tid];
+            isel[tid] = e_in;
+            wsel[tid] = w_in;
         }
     }
     // an id that cannot be used contributes nothing (the ring still streams a
@@ -518,13 +473,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     bar_compute();
     if (tid == 0) mb_arrive(&idx_ready);
 
-    // ---- phase 1: gate/up rows -> partial sums, the activations in registers ----
+    // ---- phase 1: gate/up rows -> h, the activations in registers ----
     // Warp w takes pass pw = w % NCP (chunks pw*64 + lane and pw*64 + 32 + lane
     // of every row, so its 64 activations stay in registers) and row slot
-    // w / NCP of each item; the NCP partial sums of a row meet in shared memory.
+    // w / NCP of each item.  The last of a row's NCP passes to finish adds the
+    // partial sums in pass order and stores h = SiLU(gate) * up.
     uint32_t g = 0;
-    const int p0 = (int)((long long)K * F * blockIdx.x / gridDim.x);
-    const int p1 = (int)((long long)K * F * (blockIdx.x + 1) / gridDim.x);
     {
         const int NG = D / kGroup;
         const int pw = warp % NCP, rs = warp / NCP, rstep = kWarpsC / NCP;
@@ -537,15 +491,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             xb[q] = xs4[((pw * 2 + 1) * 8 + q) * 32 + lane];
         }
         const float Xa = xc[ca], Xb = xc[cbk];
-        GuIt it;
-        for (int k = 0; gu_item(a, k, it); ++k, ++g) {
+        for (int p = p0; p < p1; ++g) {
+            const int i = p / F, j0 = p - i * F, n = min(a.r_gu, min(p1 - p, F - j0));
             const uint32_t s = g % kSlots;
             warp_wait(&full[s], (g / kSlots) & 1, a.status);
             const unsigned char *slot = ring + s * a.slot_bytes;
-            const uint32_t cb = it.n * (D / 2);
+            const uint32_t cb = n * (D / 2);
             const uint16_t *gsr = reinterpret_cast<const uint16_t *>(slot + 2 * cb);
-            const uint16_t *gbr = gsr + it.n * NG, *usr = gbr + it.n * NG, *ubr = usr + it.n * NG;
-            for (int r = rs; r < it.n; r += rstep) {
+            const uint16_t *gbr = gsr + n * NG, *usr = gbr + n * NG, *ubr = usr + n * NG;
+            for (int r = rs; r < n; r += rstep) {
                 float ag = 0.f, au = 0.f;
                 if (ca < NC) {
                     const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r * (D / 2) + ca * 16);
@@ -570,30 +524,37 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 ag = warp_sum(ag);
                 au = warp_sum(au);
                 if (lane == 0) {
-                    const int t = it.i * F + it.j0 + r - p0;     // row pair index within this CTA
-                    part[(t * NCP + pw) * 2] = ag;
-                    part[(t * NCP + pw) * 2 + 1] = au;
+                    const int t = p + r - p0;                 // row pair index within this CTA
+                    bool last = true;
+                    if (NCP > 1) {
+                        part[(t * NCP + pw) * 2] = ag;
+                        part[(t * NCP + pw) * 2 + 1] = au;
+                        __threadfence_block();
+                        last = atomicAdd(&pcnt[t], 1) == NCP - 1;
+                        if (last) {
+                            __threadfence_block();
+                            const volatile float *pv = part;
+                            ag = 0.f;
+                            au = 0.f;
+                            for (int q = 0; q < NCP; ++q) {
+                                ag += pv[(t * NCP + q) * 2];
+                                au += pv[(t * NCP + q) * 2 + 1];
+                            }
+                        }
+                    }
+                    if (last) {
+                        a.h[h_pos(i, j0 + r, MC)] = ivalid[i] ? silu_mul(ag, au) : 0.f;
+                        asm volatile("fence.proxy.async.global;" ::: "memory");   // h store -> later bulk reads
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mb_arrive(&empty[s]);
+            p += n;
         }
-    }
-    bar_compute();
-    // combine the passes of each row (fixed order) and store h where the down phase reads it
-    for (int t = tid; t < p1 - p0; t += kCompute) {
-        float ag = 0.f, au = 0.f;
-        for (int q = 0; q < NCP; ++q) {
-            ag += part[(t * NCP + q) * 2];
-            au += part[(t * NCP + q) * 2 + 1];
-        }
-        const int pp = p0 + t, i = pp / F, j = pp - i * F;
-        a.h[h_pos(i, j, MC)] = ivalid[i] ? silu_mul(ag, au) : 0.f;
     }
 
     // ---- barrier: all of h written; then one bulk copy brings it in ----
-    asm volatile("fence.proxy.async.global;" ::: "memory");   // h stores -> later bulk reads
-    __threadfence();
     grid_sync(a.gctr, a.status);
     const uint32_t hbytes = (uint32_t)(K * MC * 256 * 4);
     if (tid == 0) {
@@ -602,35 +563,55 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         bulk_g2s(hs, a.h, hbytes, &h_ready);
     }
     warp_wait(&h_ready, 0, a.status);
-    // chunk sums of h, once per CTA (each is reused by every down row of the CTA)
-    for (int q = tid; q < K * MC * 8; q += kCompute) {
-        const int i = q / (MC * 8), c = q - i * MC * 8;
-        const float4 *hp = reinterpret_cast<const float4 *>(hs) + ((i * MC + (c >> 3)) * 8) * 8 + (c & 7);
-        float sacc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 v = hp[k * 8];
-            sacc += (v.x + v.y) + (v.z + v.w);
-        }
-        hc[q] = sacc;
-    }
-    bar_compute();
 
     // ---- phase 2: down rows of this CTA ----
-    const float4 *hs4 = reinterpret_cast<const float4 *>(hs);
-    if (rows > 0) {
-        for (int i0 = 0; i0 < K; i0 += a.e_dn, ++g) {
-            const int ne = min(a.e_dn, K - i0);
-            const uint32_t s = g % kSlots;
-            warp_wait(&full[s], (g / kSlots) & 1, a.status);
-            const unsigned char *slot = ring + s * a.slot_bytes;
-            if (a.dn_sg == 8)
-                down_item<8, 2>(slot, i0, ne, rows, F, MC, hs4, hc, os, a.rows_max);
-            else
-                down_item<16, 1>(slot, i0, ne, rows, F, MC, hs4, hc, os, a.rows_max);
-            __syncwarp();
-            if (lane == 0) mb_arrive(&empty[s]);
+    // Thread t < P*RS owns (slot, chunk) pair pp = t % P -- slot i = pp / FC,
+    // chunk c = pp % FC -- and keeps that chunk of h_i in registers; it takes
+    // rows s, s+RS, ... (s = t / P) of every item.  Per row it leaves
+    // s_ic*sum((128+q)h) + (b_ic-128 s_ic)*sum(h) in red[row][pp].
+    const int RS = a.dn_rs;
+    const bool dn_live = tid < P * RS;
+    const int pp = dn_live ? tid % P : 0, sp = dn_live ? tid / P : 0;
+    const int di = pp / FC, dc = pp - di * FC;
+    float4 hq[8];
+    float Hc = 0.f;
+    {
+        const float4 *hv = reinterpret_cast<const float4 *>(hs) + ((di * MC + (dc >> 3)) * 8) * 8 + (dc & 7);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            hq[k] = hv[k * 8];
+            Hc += (hq[k].x + hq[k].y) + (hq[k].z + hq[k].w);
         }
+    }
+    bar_compute();   // h is in registers: its shared-memory region now holds red
+    for (int r0 = 0; r0 < rows; r0 += a.dn_nr, ++g) {
+        const int nr = min(a.dn_nr, rows - r0);
+        const uint32_t s = g % kSlots;
+        warp_wait(&full[s], (g / kSlots) & 1, a.status);
+        const unsigned char *slot = ring + s * a.slot_bytes;
+        if (dn_live) {
+            const uint32_t cb = nr * (F / 2), sb = nr * FG * 2;
+            const unsigned char *cp = slot + di * cb + dc * 16;
+            const uint16_t *sp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + di * sb) + (dc >> 1);
+            const uint16_t *bp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + (K + di) * sb) + (dc >> 1);
+            for (int rr = sp; rr < nr; rr += RS) {
+                const uint4 cv = *reinterpret_cast<const uint4 *>(cp + rr * (F / 2));
+                const float A = dot32(cv, hq);
+                const float sc = bf16_to_f32(sp16[rr * FG]), bi = bf16_to_f32(bp16[rr * FG]);
+                red[(r0 + rr) * P + pp] = sc * A + (bi - 128.f * sc) * Hc;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mb_arrive(&empty[s]);
+    }
+    bar_compute();
+    // o_i[r]: the FC chunk partials of slot i, in chunk order
+    for (int u = tid; u < rows * K; u += kCompute) {
+        const int r = u / K, i = u - r * K;
+        const float *rp = red + r * P + i * FC;
+        float o = 0.f;
+        for (int c = 0; c < FC; ++c) o += rp[c];
+        os[i * a.rows_max + r] = o;
     }
     bar_compute();
     for (int r = tid; r < rows; r += kCompute) {
@@ -656,39 +637,37 @@ bool fused_plan(FusedArgs &a, int num_sms) {
         if (reinterpret_cast<uintptr_t>(q) % 16) return false;
     if (a.gain && reinterpret_cast<uintptr_t>(a.gain) % 16) return false;
     a.grid = num_sms;
-    if (a.E > a.grid) return false;
-    const int NG = D / kGroup, FG = F / kGroup;
+    if (a.E > a.grid || a.grid > 256) return false;
+    const int NG = D / kGroup, FG = F / kGroup, FC = F / 32;
+    // down: the (slot, chunk) pairs must fit the compute threads (h in registers)
+    const int P = K * FC;
+    if (P > kCompute) return false;
+    a.dn_rs = kCompute / P;
+    // row blocks whose scale rows start 16-byte aligned
     int gran = 1;
-    while ((gran * (F / 32)) % 16) ++gran;
+    while ((gran * FC) % 16) ++gran;
     a.dn_gran = gran;
     const int units = D / gran;
     a.rows_max = ((units + a.grid - 1) / a.grid) * gran;
     const int row_pair_bytes = 2 * (D / 2 + NG * 2 * 2);
-    const int dn_bytes_1 = a.rows_max * (F / 2 + FG * 2 * 2);
+    const int dn_row_bytes = K * (F / 2 + FG * 2 * 2);       // one down row, all K slots
     // gate/up: one row pair per (group of NCP warps) per item
     const int NCPh = (D / 32 + 63) / 64;
     a.r_gu = kWarpsC / NCPh;
     while (a.r_gu > 1 && a.r_gu * row_pair_bytes > kSlotMax) --a.r_gu;
-    // down: as many experts per item as fit in a slot
-    a.e_dn = kSlotMax / dn_bytes_1;
-    if (a.e_dn > K) a.e_dn = K;
-    if (a.e_dn < 1) return false;
-    // subgroup width: 8 lanes x 2 rows, or 16 lanes x 1 row -- fewer rounds x chunks wins
-    {
-        const int FCh = F / 32;
-        const int units8 = a.e_dn * ((a.rows_max + 1) / 2), units16 = a.e_dn * a.rows_max;
-        const int cost8 = ((units8 + kWarpsC * 4 - 1) / (kWarpsC * 4)) * ((FCh + 7) / 8) * 2;
-        const int cost16 = ((units16 + kWarpsC * 2 - 1) / (kWarpsC * 2)) * ((FCh + 15) / 16);
-        a.dn_sg = cost16 < cost8 ? 16 : 8;
-    }
-    a.slot_bytes = max(a.r_gu * row_pair_bytes, a.e_dn * dn_bytes_1);
+    // down: as many rows (multiples of gran) per item as fit in a slot
+    a.dn_nr = (kSlotMax / dn_row_bytes) / gran * gran;
+    if (a.dn_nr < gran) return false;
+    if (a.dn_nr > a.rows_max) a.dn_nr = a.rows_max;
+    a.slot_bytes = max(a.r_gu * row_pair_bytes, a.dn_nr * dn_row_bytes);
     a.slot_bytes = (a.slot_bytes + 127) / 128 * 128;
     a.ring_bytes = kSlots * a.slot_bytes;
-    const int NCP = (D / 32 + 63) / 64, MC = (F / 32 + 7) / 8;
+    const int NCP = (D / 32 + 63) / 64, MC = (FC + 7) / 8;
     const int xs_bytes = (NCP * 2048 + NCP * 64) * 4;
-    const int hs_bytes = (K * MC * 256 + K * MC * 8) * 4;
+    const int hs_bytes = K * MC * 256 * 4;
+    const int red_bytes = a.rows_max * P * 4;
     if ((K * F + a.grid - 1) / a.grid > kMaxGuRows || D / 32 > 128) return false;
-    a.union_bytes = (max(xs_bytes, hs_bytes) + 127) / 128 * 128;
+    a.union_bytes = (max(xs_bytes, max(hs_bytes, red_bytes)) + 127) / 128 * 128;
     a.smem_bytes = a.ring_bytes + a.union_bytes + D * 2 + K * a.rows_max * 4;
     return a.smem_bytes <= 210 * 1024;
 }

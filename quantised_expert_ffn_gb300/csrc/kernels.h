@@ -96,7 +96,7 @@ struct FusedArgs {
     const float *w_in;          // [K]
     float *expert_out;          // [K][D] or NULL
     // plan (fused_plan)
-    int grid, r_gu, e_dn, dn_gran, dn_sg, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
+    int grid, r_gu, dn_nr, dn_gran, dn_rs, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
 };
 bool fused_plan(FusedArgs &a, int num_sms);
 size_t fused_h_floats(int F, int K);

@@ -39,6 +39,10 @@ SHAPES = {
     "odd": (192, 24, 3, 320),        # D/64 = 3 groups, F/32 = 10 chunks: ragged lanes
     "30b": (2048, 128, 8, 768),
     "235b": (4096, 128, 8, 1536),
+    # one-kernel decode layer at its edges: D/32 chunks not a multiple of 64
+    # (idle lanes in the gate/up sweep), F/32 = 12 and 4 chunks per down row
+    "f1536": (1536, 64, 6, 384),
+    "f512": (512, 16, 4, 128),
 }
 _cache = {}
 
@@ -178,7 +182,8 @@ def test_expert_union_bad_ids_set_status(smoe, orc):
 # ------------------------------------------------------------------------- decode
 
 @pytest.mark.parametrize("name,norm,ntok", [("tiny", False, 6), ("odd", True, 4), ("30b", False, 6),
-                                            ("30b", True, 6), ("235b", True, 3)])
+                                            ("30b", True, 6), ("235b", True, 3), ("f1536", True, 3),
+                                            ("f512", False, 3)])
 def test_moe_decode(smoe, orc, name, norm, ntok):
     W, OL = layer(name, norm)
     D, K = W.d_model, W.top_k
@@ -198,6 +203,35 @@ def test_moe_decode(smoe, orc, name, norm, ntok):
         np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
         assert max_row_rel_l2(host(eo), ref["expert_out"]) <= TOL
         assert rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+    assert smoe.smoe_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("name,ids", [("30b", "distinct"), ("235b", "distinct"), ("f1536", "repeat"),
+                                      ("f512", "distinct")])
+def test_moe_ffn_decode_given_ids(smoe, orc, name, ids):
+    """Expert FFN with caller-given ids and weights: y = x + sum_i w_i o_i and
+    every o_i against the oracle's expert FFN on the normed input."""
+    W, OL = layer(name, True)
+    D, E, K = W.d_model, W.n_experts, W.top_k
+    rng = np.random.default_rng(77)
+    x = bits(synth.hidden(1, D, seed=31))[0]
+    if ids == "distinct":
+        idx = rng.choice(E, K, replace=False).astype(np.int32)
+    else:                                             # the same expert in several slots
+        idx = rng.choice(E, K, replace=True).astype(np.int32)
+        idx[1] = idx[0]
+    w = rng.uniform(0.05, 1.0, K).astype(np.float32)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 1)
+    y = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+    eo = torch.empty((K, D), dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_ffn_decode(L, dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), y, eo, ws)
+    torch.cuda.synchronize()
+    xn = orc.rmsnorm(OL, x)
+    o = np.stack([orc.expert_ffn(OL, int(e), xn)[0] for e in idx])
+    assert max_row_rel_l2(host(eo), o) <= TOL
+    y_ref = bf16_f64(x) + (w.astype(np.float64)[:, None] * o).sum(0)
+    assert rel_l2(bf16_f64(host(y)), y_ref) <= TOL
     assert smoe.smoe_read_device_status(ws) == 0
 
 
