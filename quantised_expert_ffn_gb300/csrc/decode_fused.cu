@@ -46,6 +46,7 @@ constexpr int kThreadsF = kCompute + 32;       // + producer warp
 constexpr int kSlots = 3;
 constexpr int kSlotMax = 48 * 1024 + 512;     // largest ring slot
 constexpr int kMaxGuRows = 128;                // gate/up row pairs per CTA
+constexpr int kDnU = 7;                        // down rows per thread per ring item
 
 // ---------------------------------------------------------------- primitives
 
@@ -76,13 +77,14 @@ __device__ __forceinline__ bool mb_try(uint64_t *b, uint32_t par) {
         : "memory");
     return ok;
 }
-// Wait for the phase of parity `par`, bounded in wall time; the thread sleeps
-// in hardware between tries.
+// Wait for the phase of parity `par`, bounded in wall time.  try_wait without
+// a suspend hint: each try blocks for the hardware's own short window, and a
+// completed phase is seen at once (a long suspend hint wakes threads late).
 __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t par, int32_t *status) {
     if (mb_try(b, par)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_suspend(su32(b), par, kSuspendHintNs)) return true;
+        if (mb_try(b, par)) return true;
         if (global_ns() - t0 > kWaitLimitNs) break;
     }
     set_status(status, SMOE_ERR_TIMEOUT);
@@ -204,7 +206,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     __shared__ float lsel[kMaxTopK], wsel[kMaxTopK];
     __shared__ int isel[kMaxTopK], ivalid[kMaxTopK];
     __shared__ float part[kMaxGuRows * 2 * 2];   // gate/up partial sums per (row, pass)
-    __shared__ int pcnt[kMaxGuRows];             // passes of a row done
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) {
@@ -216,7 +217,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         mb_init(&h_ready, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < kMaxGuRows) pcnt[tid] = 0;
     __syncthreads();
 
     int d0, d1, p0, p1;
@@ -227,11 +227,25 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     if (warp == kWarpsC) {
         // ================= producer: bulk copies into the ring =================
         // Lane 0 waits for a free slot and posts its byte count; then one lane
-        // per copy issues the copies of the item together.
-        int ok = 1;
-        if (lane == 0) ok = mb_wait(&idx_ready, 0, a.status);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-        mb_try(&idx_ready, 0);                 // each lane observes the ids
+        // per copy issues the copies of the item together.  Lane i < K holds
+        // the expert of slot i: the ranked id, or -- given ids -- read here as
+        // soon as the previous kernel is done, so streaming starts while the
+        // compute warps still normalise x (an id that cannot be used streams
+        // expert 0, as on the compute side).
+        int my_e = 0;
+        if (kRoute) {
+            int ok = 1;
+            if (lane == 0) ok = mb_wait(&idx_ready, 0, a.status);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+            mb_try(&idx_ready, 0);                 // each lane observes the ids
+            if (lane < K) my_e = isel[lane];
+        } else {
+            pdl_wait();
+            if (lane < K) {
+                const int e = __ldcg(a.idx_in + lane);
+                my_e = (e >= 0 && e < E) ? e : 0;
+            }
+        }
         const int NG = D / kGroup;
         uint32_t g = 0;
         for (int p = p0; p < p1; ++g) {
@@ -245,7 +259,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             }
             __syncwarp();
             mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
-            const size_t row = (size_t)isel[i] * F + j0;
+            const size_t row = (size_t)__shfl_sync(0xffffffffu, my_e, i) * F + j0;
             if (lane < 2) {
                 bulk_g2s(dst + lane * cb, (lane ? a.uq : a.gq) + row * (D / 2), cb, &full[s]);
             } else if (lane < 6) {
@@ -265,9 +279,11 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             }
             __syncwarp();
             mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
+            const int e_lo = __shfl_sync(0xffffffffu, my_e, lane % K);
+            const int e_hi = __shfl_sync(0xffffffffu, my_e, (lane + 32) % K);
             for (int q = lane; q < 3 * K; q += 32) {
                 const int i = q % K, kind = q / K;
-                const size_t row = (size_t)isel[i] * D + d0 + r0;
+                const size_t row = (size_t)(q < 32 ? e_lo : e_hi) * D + d0 + r0;
                 if (kind == 0)
                     bulk_g2s(dst + i * cb, a.dq + row * (F / 2), cb, &full[s]);
                 else
@@ -476,8 +492,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     // ---- phase 1: gate/up rows -> h, the activations in registers ----
     // Warp w takes pass pw = w % NCP (chunks pw*64 + lane and pw*64 + 32 + lane
     // of every row, so its 64 activations stay in registers) and row slot
-    // w / NCP of each item.  The last of a row's NCP passes to finish adds the
-    // partial sums in pass order and stores h = SiLU(gate) * up.
+    // w / NCP of each item; the NCP partial sums of a row meet in shared memory.
     uint32_t g = 0;
     {
         const int NG = D / kGroup;
@@ -525,27 +540,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 au = warp_sum(au);
                 if (lane == 0) {
                     const int t = p + r - p0;                 // row pair index within this CTA
-                    bool last = true;
-                    if (NCP > 1) {
-                        part[(t * NCP + pw) * 2] = ag;
-                        part[(t * NCP + pw) * 2 + 1] = au;
-                        __threadfence_block();
-                        last = atomicAdd(&pcnt[t], 1) == NCP - 1;
-                        if (last) {
-                            __threadfence_block();
-                            const volatile float *pv = part;
-                            ag = 0.f;
-                            au = 0.f;
-                            for (int q = 0; q < NCP; ++q) {
-                                ag += pv[(t * NCP + q) * 2];
-                                au += pv[(t * NCP + q) * 2 + 1];
-                            }
-                        }
-                    }
-                    if (last) {
-                        a.h[h_pos(i, j0 + r, MC)] = ivalid[i] ? silu_mul(ag, au) : 0.f;
-                        asm volatile("fence.proxy.async.global;" ::: "memory");   // h store -> later bulk reads
-                    }
+                    part[(t * NCP + pw) * 2] = ag;
+                    part[(t * NCP + pw) * 2 + 1] = au;
                 }
             }
             __syncwarp();
@@ -554,61 +550,93 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         }
     }
 
-    // ---- barrier: all of h written; then one bulk copy brings it in ----
-    grid_sync(a.gctr, a.status);
-    const uint32_t hbytes = (uint32_t)(K * MC * 256 * 4);
-    if (tid == 0) {
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        mb_expect(&h_ready, hbytes);
-        bulk_g2s(hs, a.h, hbytes, &h_ready);
-    }
-    warp_wait(&h_ready, 0, a.status);
-
-    // ---- phase 2: down rows of this CTA ----
+    // ---- phase 2 set-up: down rows of this CTA ----
     // Thread t < P*RS owns (slot, chunk) pair pp = t % P -- slot i = pp / FC,
     // chunk c = pp % FC -- and keeps that chunk of h_i in registers; it takes
     // rows s, s+RS, ... (s = t / P) of every item.  Per row it leaves
-    // s_ic*sum((128+q)h) + (b_ic-128 s_ic)*sum(h) in red[row][pp].
+    // s_ic*sum((128+q)h) + (b_ic-128 s_ic)*sum(h) in red[(row*K + i)*(FC+1) + c]
+    // (rows of FC+1 floats: the later per-(row, slot) sums read without bank
+    // conflicts).
     const int RS = a.dn_rs;
     const bool dn_live = tid < P * RS;
     const int pp = dn_live ? tid % P : 0, sp = dn_live ? tid / P : 0;
     const int di = pp / FC, dc = pp - di * FC;
     float4 hq[8];
-    float Hc = 0.f;
-    {
-        const float4 *hv = reinterpret_cast<const float4 *>(hs) + ((di * MC + (dc >> 3)) * 8) * 8 + (dc & 7);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            hq[k] = hv[k * 8];
-            Hc += (hq[k].x + hq[k].y) + (hq[k].z + hq[k].w);
-        }
-    }
-    bar_compute();   // h is in registers: its shared-memory region now holds red
-    for (int r0 = 0; r0 < rows; r0 += a.dn_nr, ++g) {
-        const int nr = min(a.dn_nr, rows - r0);
-        const uint32_t s = g % kSlots;
-        warp_wait(&full[s], (g / kSlots) & 1, a.status);
-        const unsigned char *slot = ring + s * a.slot_bytes;
-        if (dn_live) {
-            const uint32_t cb = nr * (F / 2), sb = nr * FG * 2;
-            const unsigned char *cp = slot + di * cb + dc * 16;
-            const uint16_t *sp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + di * sb) + (dc >> 1);
-            const uint16_t *bp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + (K + di) * sb) + (dc >> 1);
-            for (int rr = sp; rr < nr; rr += RS) {
-                const uint4 cv = *reinterpret_cast<const uint4 *>(cp + rr * (F / 2));
-                const float A = dot32(cv, hq);
-                const float sc = bf16_to_f32(sp16[rr * FG]), bi = bf16_to_f32(bp16[rr * FG]);
-                red[(r0 + rr) * P + pp] = sc * A + (bi - 128.f * sc) * Hc;
+    for (int k = 0; k < 8; ++k) hq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Hc = 0.f;
+
+    // Pass 0 runs the down-row code once on whatever the first ring slot
+    // holds and keeps nothing: a warp that is done with gate/up fetches those
+    // instructions while it would otherwise wait at the barrier.  Pass 1 is
+    // the real one.
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool real = pass == 1;
+        if (real) {
+            bar_compute();
+            // the passes of each gate/up row, added in pass order: h = SiLU(gate) * up
+            for (int t = tid; t < p1 - p0; t += kCompute) {
+                float ag = 0.f, au = 0.f;
+                for (int q = 0; q < NCP; ++q) {
+                    ag += part[(t * NCP + q) * 2];
+                    au += part[(t * NCP + q) * 2 + 1];
+                }
+                const int pq = p0 + t, i = pq / F, j = pq - i * F;
+                a.h[h_pos(i, j, MC)] = ivalid[i] ? silu_mul(ag, au) : 0.f;
+                asm volatile("fence.proxy.async.global;" ::: "memory");   // h store -> later bulk reads
             }
+            // ---- barrier: all of h written; then one bulk copy brings it in ----
+            grid_sync(a.gctr, a.status);
+            const uint32_t hbytes = (uint32_t)(K * MC * 256 * 4);
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                mb_expect(&h_ready, hbytes);
+                bulk_g2s(hs, a.h, hbytes, &h_ready);
+            }
+            warp_wait(&h_ready, 0, a.status);
+            const float4 *hv = reinterpret_cast<const float4 *>(hs) + ((di * MC + (dc >> 3)) * 8) * 8 + (dc & 7);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                hq[k] = hv[k * 8];
+                Hc += (hq[k].x + hq[k].y) + (hq[k].z + hq[k].w);
+            }
+            bar_compute();   // h is in registers: its shared-memory region now holds red
         }
-        __syncwarp();
-        if (lane == 0) mb_arrive(&empty[s]);
+        for (int r0 = 0; r0 < rows; r0 += a.dn_nr) {
+            const int nr = min(a.dn_nr, rows - r0);
+            const uint32_t s = g % kSlots;
+            if (real) warp_wait(&full[s], (g / kSlots) & 1, a.status);
+            const unsigned char *slot = ring + (real ? s : 0) * a.slot_bytes;
+            if (dn_live && sp < nr) {
+                const uint32_t cb = nr * (F / 2), sb = nr * FG * 2;
+                const unsigned char *cp = slot + di * cb + dc * 16;
+                const uint16_t *sp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + di * sb) + (dc >> 1);
+                const uint16_t *bp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + (K + di) * sb) + (dc >> 1);
+                float acc[kDnU];
+#pragma unroll
+                for (int u = 0; u < kDnU; ++u) {
+                    const int rr = min(sp + u * RS, nr - 1);          // a row past the item repeats the last
+                    const uint4 cv = *reinterpret_cast<const uint4 *>(cp + rr * (F / 2));
+                    const float A = dot32(cv, hq);
+                    const float sc = bf16_to_f32(sp16[rr * FG]), bi = bf16_to_f32(bp16[rr * FG]);
+                    acc[u] = sc * A + (bi - 128.f * sc) * Hc;
+                }
+#pragma unroll
+                for (int u = 0; u < kDnU; ++u)
+                    if (real && sp + u * RS < nr) red[((r0 + sp + u * RS) * K + di) * (FC + 1) + dc] = acc[u];
+            }
+            __syncwarp();
+            if (!real) break;
+            if (lane == 0) mb_arrive(&empty[s]);
+            ++g;
+        }
     }
     bar_compute();
     // o_i[r]: the FC chunk partials of slot i, in chunk order
     for (int u = tid; u < rows * K; u += kCompute) {
         const int r = u / K, i = u - r * K;
-        const float *rp = red + r * P + i * FC;
+        const float *rp = red + (r * K + i) * (FC + 1);
         float o = 0.f;
         for (int c = 0; c < FC; ++c) o += rp[c];
         os[i * a.rows_max + r] = o;
@@ -657,6 +685,7 @@ bool fused_plan(FusedArgs &a, int num_sms) {
     while (a.r_gu > 1 && a.r_gu * row_pair_bytes > kSlotMax) --a.r_gu;
     // down: as many rows (multiples of gran) per item as fit in a slot
     a.dn_nr = (kSlotMax / dn_row_bytes) / gran * gran;
+    a.dn_nr = min(a.dn_nr, kDnU * a.dn_rs / gran * gran);   // each thread's rows of an item unroll fully
     if (a.dn_nr < gran) return false;
     if (a.dn_nr > a.rows_max) a.dn_nr = a.rows_max;
     a.slot_bytes = max(a.r_gu * row_pair_bytes, a.dn_nr * dn_row_bytes);
@@ -665,7 +694,7 @@ bool fused_plan(FusedArgs &a, int num_sms) {
     const int NCP = (D / 32 + 63) / 64, MC = (FC + 7) / 8;
     const int xs_bytes = (NCP * 2048 + NCP * 64) * 4;
     const int hs_bytes = K * MC * 256 * 4;
-    const int red_bytes = a.rows_max * P * 4;
+    const int red_bytes = a.rows_max * K * (FC + 1) * 4;
     if ((K * F + a.grid - 1) / a.grid > kMaxGuRows || D / 32 > 128) return false;
     a.union_bytes = (max(xs_bytes, max(hs_bytes, red_bytes)) + 127) / 128 * 128;
     a.smem_bytes = a.ring_bytes + a.union_bytes + D * 2 + K * a.rows_max * 4;
