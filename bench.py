@@ -40,6 +40,8 @@ METRIC = ("MoE decode tokens/s (b=1) + expert-FFN effective HBM GB/s vs peak; pr
 D30, E, K, F30, L30 = 2048, 128, 8, 768, 48
 D235, F235, L235 = 4096, 1536, 94
 SEED = 1337
+PER_LAYER = False   # --per-layer: decode through one smoe_moe_decode call per layer
+
 # sources of the kernel the roofline reports (the fused decode layer, FFN-only variant)
 FFN_SOURCES = ["quantised_expert_ffn_gb300/csrc/decode_fused.cu",
                "quantised_expert_ffn_gb300/csrc/common.cuh",
@@ -171,12 +173,18 @@ class DecodeStack:
         self.W = [synth.layer_weights(D, E, F, K, seed=seed * 1000 + i, device=dev, rms_norm=True)
                   for i in range(n_layers)]
         self.L = [smoe.Layer(w) for w in self.W]
+        self.table = smoe.LayerTable(self.L, dev)
         self.ws = smoe.workspace(self.L[0], 64)
         self.D, self.F, self.n = D, F, n_layers
         self.bufs = [torch.empty(D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.per_layer = PER_LAYER
 
     def token(self, x_in, y_out):
-        """One token through all layers: x_in -> ... -> y_out (ping-pong in between)."""
+        """One token through all layers: one launch (smoe_moe_decode_layers), or
+        with --per-layer one smoe_moe_decode call per layer (ping-pong buffers)."""
+        if not self.per_layer:
+            self.smoe.smoe_moe_decode_layers(self.table, x_in, y_out, ws=self.ws)
+            return
         cur = x_in
         for i, L in enumerate(self.L):
             nxt = y_out if i == self.n - 1 else self.bufs[i % 2]
@@ -428,19 +436,30 @@ def our_arm(args):
                        "graph_tokens": batch},
             "effective_gbs_per_token": round(bytes_token / (ms_tok / 1e3) / 1e9, 1),
             "clocks": clocks,
-            "gpu_launches": args.steps * L30 * 3}
+            "gpu_launches": args.steps * (L30 if PER_LAYER else 1)}
+    line["config"]["decode_launches_per_token"] = L30 if PER_LAYER else 1
 
     if rank == 0:
-        # ---- roofline of the dominant work: the decode expert FFN call
-        ffn_ms = time_ffn(stack, states, 8)
-        ffn_bytes = K * expert_bytes(D30, F30)
-        achieved = ffn_bytes / (ffn_ms / 1e3) / 1e9
-        traffic = traffic_from_profile("decode_ffn_30b", FFN_SOURCES)
+        # ---- roofline of the dominant kernel: the decode step's one launch per
+        # token (all 48 layers), timed by the graph replays above
+        achieved = bytes_token / (ms_tok / 1e3) / 1e9
+        traffic = traffic_from_profile("decode_stack_30b", FFN_SOURCES)
+        if traffic is not None:
+            traffic = round(traffic * L30, 0)      # profiled per layer; traffic grows with layers
+        kname = ("k_decode_layer, one launch per layer (route + gate/up + down + residual)" if PER_LAYER
+                 else "k_decode_layer, one launch per token over 48 layers (route + gate/up + down + residual)")
         line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                             "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                            "traffic": traffic, "peak_kind": peak_kind,
-                            "kernel": "k_decode_layer (FFN only: gate/up + down + residual), 8 experts",
-                            "bytes_per_launch": ffn_bytes, "ms_per_launch": round(ffn_ms, 5)}
+                            "traffic": traffic, "peak_kind": peak_kind, "kernel": kname,
+                            "bytes_per_launch": bytes_token // (L30 if PER_LAYER else 1),
+                            "ms_per_launch": round(ms_tok / (L30 if PER_LAYER else 1), 5)}
+        # ---- the expert FFN call alone (FFN-only variant, ids given), per layer
+        ffn_ms = time_ffn(stack, states, 8)
+        ffn_bytes = K * expert_bytes(D30, F30)
+        line["ffn_call"] = {"kernel": "k_decode_layer (FFN only: gate/up + down + residual), 8 experts",
+                            "bytes": ffn_bytes, "ms": round(ffn_ms, 5),
+                            "gbs": round(ffn_bytes / (ffn_ms / 1e3) / 1e9, 1),
+                            "frac": round(ffn_bytes / (ffn_ms / 1e3) / 1e9 / hbm_peak, 4)}
         # ---- end to end through the C ABI with host buffers
         states_host = states[:64].cpu().pin_memory()
         e2e, bi, bo = time_e2e(stack, states_host, args.steps, max(3, args.warmup))
@@ -537,11 +556,15 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=16)
     ap.add_argument("--cpu-layers", type=int, default=4)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="decode with one launch per layer instead of one per token")
     ap.add_argument("--no-235b", action="store_true")
     ap.add_argument("--profile-layers", type=int, default=0,
                     help="run only the small ncu case with this many layers")
     ap.add_argument("--profile-shape", default="30b", choices=["30b", "235b"])
     args = ap.parse_args()
+    global PER_LAYER
+    PER_LAYER = args.per_layer
     if args.profile_layers:
         profile_case(args)
         return

@@ -187,6 +187,28 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
                            int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
                            smoe_stream stream);
 
+/* One decode token through n_layers routed-MoE layers, each as
+ * smoe_moe_decode computes it, in ONE kernel launch ("Optimizations" page,
+ * "The Dense Ceiling -- GPU-Resident Epilogue": the per-token work stays on
+ * the GPU; here the layers of the token do too, with grid-wide barriers
+ * between them instead of kernel boundaries).
+ *   layers      HOST array of n_layers layers: checked on the host (shapes,
+ *               pointers, alignment); all layers must share d_model,
+ *               n_experts, top_k, ffn_dim, norm_topk_prob, rms_eps and the
+ *               presence of rms_gain.
+ *   layers_dev  DEVICE copy of the same array (caller-owned, same contents,
+ *               8-byte aligned); the kernel reads the weight pointers there.
+ *   x, y        bf16 [D]; y may alias x.  The activations between layers live
+ *               in the workspace (smoe_workspace_bytes(&layers[0], 1)).
+ *   idx_out_opt int32 [n_layers][k] and w_out_opt fp32 [n_layers][k]: both or
+ *               neither.
+ * Results equal n_layers chained smoe_moe_decode calls bit for bit.  Layers
+ * whose weights are not 16-byte aligned, or a shape the one-kernel plan does
+ * not take, run as one launch sequence per layer with the same results. */
+int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_dev, int n_layers,
+                           const smoe_bf16 *x, smoe_bf16 *y, int32_t *idx_out_opt,
+                           float *w_out_opt, void *ws, size_t ws_bytes, smoe_stream stream);
+
 /* Decode without a workspace.  The pages have no counterpart of this call:
  * it exists for callers that cannot allocate device memory when they run a
  * layer -- real-time loops whose latency budget rules out the device-wide

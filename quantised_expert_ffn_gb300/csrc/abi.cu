@@ -220,6 +220,7 @@ static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int
     f.idx_in = idx_in;
     f.w_in = w_in;
     f.expert_out = expert_out;
+    f.n_layers = 1;
     if (decode_path() == 1 && fused_plan(f, device_sm_count()))
         return cuda_status(launch_decode_layer(f, s, idx_in == nullptr));
     if (!idx_in) {
@@ -276,6 +277,72 @@ int smoe_moe_decode(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
     float *w = w_out_opt ? w_out_opt : at<float>(ws, o.w);
     return launch_decode_path(*layer, x, nullptr, nullptr, idx, w, y, expert_out_opt, ws, o,
                               (cudaStream_t)stream);
+}
+
+int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_dev, int n_layers,
+                           const smoe_bf16 *x, smoe_bf16 *y, int32_t *idx_out_opt, float *w_out_opt,
+                           void *ws, size_t ws_bytes, smoe_stream stream) {
+    if (!layers || !layers_dev || n_layers < 1 || !aligned(layers_dev, alignof(smoe_layer)))
+        return SMOE_ERR_INVALID_ARG;
+    if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return SMOE_ERR_INVALID_ARG;
+    if ((idx_out_opt == nullptr) != (w_out_opt == nullptr)) return SMOE_ERR_INVALID_ARG;
+    const smoe_layer &L0 = layers[0];
+    bool stack_ok = true;     // every layer meets the one-kernel plan's alignment
+    for (int l = 0; l < n_layers; ++l) {
+        const smoe_layer &L = layers[l];
+        const int st = check_layer(&L);
+        if (st != SMOE_OK) return st;
+        if (L.d_model != L0.d_model || L.n_experts != L0.n_experts || L.top_k != L0.top_k ||
+            L.ffn_dim != L0.ffn_dim || L.norm_topk_prob != L0.norm_topk_prob ||
+            (L.rms_gain == nullptr) != (L0.rms_gain == nullptr) || L.rms_eps != L0.rms_eps)
+            return SMOE_ERR_INVALID_ARG;
+        const void *ptrs[] = {L.router_w, L.gate_q, L.gate_s, L.gate_b, L.up_q, L.up_s, L.up_b,
+                              L.down_q, L.down_s, L.down_b};
+        for (const void *q : ptrs) stack_ok = stack_ok && aligned(q, 16);
+        if (L.rms_gain) stack_ok = stack_ok && aligned(L.rms_gain, 16);
+    }
+    int st = check_ws(&L0, 1, ws, ws_bytes);
+    if (st != SMOE_OK) return st;
+    const WsLayout o = ws_layout(L0, 1);
+    cudaStream_t s = (cudaStream_t)stream;
+    smoe_bf16 *act[2] = {at<smoe_bf16>(ws, o.xn), at<smoe_bf16>(ws, o.xn16)};
+    if (stack_ok && decode_path() == 1) {
+        FusedArgs f{};
+        f.x = x;
+        f.y = y;
+        f.gain = L0.rms_gain;
+        f.eps = L0.rms_eps;
+        f.D = L0.d_model;
+        f.F = L0.ffn_dim;
+        f.K = L0.top_k;
+        f.E = L0.n_experts;
+        f.norm_topk_prob = L0.norm_topk_prob ? 1 : 0;
+        f.router_w = L0.router_w;
+        f.gq = L0.gate_q; f.gs = L0.gate_s; f.gb = L0.gate_b;
+        f.uq = L0.up_q;   f.us = L0.up_s;   f.ub = L0.up_b;
+        f.dq = L0.down_q; f.ds = L0.down_s; f.db = L0.down_b;
+        f.logits = at<float>(ws, o.logits);
+        f.h = at<float>(ws, o.h);
+        f.gctr = at<unsigned long long>(ws, o.gbar);
+        f.status = at<int32_t>(ws, o.status);
+        f.idx_out = idx_out_opt;
+        f.w_out = w_out_opt;
+        f.layers = layers_dev;
+        f.n_layers = n_layers;
+        f.act0 = act[0];
+        f.act1 = act[1];
+        if (fused_plan(f, device_sm_count())) return cuda_status(launch_decode_layer(f, s, true));
+    }
+    // one launch sequence per layer, activations ping-ponging in the workspace
+    for (int l = 0; l < n_layers; ++l) {
+        const smoe_bf16 *xin = l == 0 ? x : act[(l - 1) & 1];
+        smoe_bf16 *yout = l == n_layers - 1 ? y : act[l & 1];
+        int32_t *idx = idx_out_opt ? idx_out_opt + (size_t)l * L0.top_k : at<int32_t>(ws, o.idx);
+        float *w = w_out_opt ? w_out_opt + (size_t)l * L0.top_k : at<float>(ws, o.w);
+        st = launch_decode_path(layers[l], xin, nullptr, nullptr, idx, w, yout, nullptr, ws, o, s);
+        if (st != SMOE_OK) return st;
+    }
+    return SMOE_OK;
 }
 
 int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,

@@ -180,6 +180,19 @@ __device__ __forceinline__ int h_pos(int i, int f, int MC) {
     return ((((i * MC + (c >> 3)) * 8 + k) * 8 + (c & 7)) << 2) + (f & 3);
 }
 
+// Weights of layer l: the stack variant reads them from the device table.
+struct LW {
+    const uint16_t *gain, *router_w;
+    const uint8_t *gq, *uq, *dq;
+    const uint16_t *gs, *gb, *us, *ub, *ds, *db;
+};
+__device__ __forceinline__ LW layer_w(const FusedArgs &a, int l) {
+    if (!a.layers) return {a.gain, a.router_w, a.gq, a.uq, a.dq, a.gs, a.gb, a.us, a.ub, a.ds, a.db};
+    const smoe_layer *L = a.layers + l;
+    return {L->rms_gain, L->router_w, L->gate_q, L->up_q, L->down_q, L->gate_s, L->gate_b,
+            L->up_s, L->up_b, L->down_s, L->down_b};
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <bool kRoute>
@@ -232,12 +245,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         // soon as the previous kernel is done, so streaming starts while the
         // compute warps still normalise x (an id that cannot be used streams
         // expert 0, as on the compute side).
+        uint32_t g = 0;
+        for (int l = 0; l < a.n_layers; ++l) {
+        const LW W = layer_w(a, l);
         int my_e = 0;
         if (kRoute) {
             int ok = 1;
-            if (lane == 0) ok = mb_wait(&idx_ready, 0, a.status);
+            if (lane == 0) ok = mb_wait(&idx_ready, l & 1, a.status);
             if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-            mb_try(&idx_ready, 0);                 // each lane observes the ids
+            mb_try(&idx_ready, l & 1);             // each lane observes the ids
             if (lane < K) my_e = isel[lane];
         } else {
             pdl_wait();
@@ -247,7 +263,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             }
         }
         const int NG = D / kGroup;
-        uint32_t g = 0;
         for (int p = p0; p < p1; ++g) {
             const int i = p / F, j0 = p - i * F, n = min(a.r_gu, min(p1 - p, F - j0));
             const uint32_t s = g % kSlots;
@@ -261,9 +276,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
             const size_t row = (size_t)__shfl_sync(0xffffffffu, my_e, i) * F + j0;
             if (lane < 2) {
-                bulk_g2s(dst + lane * cb, (lane ? a.uq : a.gq) + row * (D / 2), cb, &full[s]);
+                bulk_g2s(dst + lane * cb, (lane ? W.uq : W.gq) + row * (D / 2), cb, &full[s]);
             } else if (lane < 6) {
-                const uint16_t *src = lane == 2 ? a.gs : lane == 3 ? a.gb : lane == 4 ? a.us : a.ub;
+                const uint16_t *src = lane == 2 ? W.gs : lane == 3 ? W.gb : lane == 4 ? W.us : W.ub;
                 bulk_g2s(dst + 2 * cb + (lane - 2) * sb, src + row * NG, sb, &full[s]);
             }
             p += n;
@@ -285,12 +300,13 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 const int i = q % K, kind = q / K;
                 const size_t row = (size_t)(q < 32 ? e_lo : e_hi) * D + d0 + r0;
                 if (kind == 0)
-                    bulk_g2s(dst + i * cb, a.dq + row * (F / 2), cb, &full[s]);
+                    bulk_g2s(dst + i * cb, W.dq + row * (F / 2), cb, &full[s]);
                 else
-                    bulk_g2s(dst + K * cb + ((kind - 1) * K + i) * sb, (kind == 1 ? a.ds : a.db) + row * FG, sb,
+                    bulk_g2s(dst + K * cb + ((kind - 1) * K + i) * sb, (kind == 1 ? W.ds : W.db) + row * FG, sb,
                              &full[s]);
             }
         }
+        }   // layers
         // every copy issued has landed before the CTA may exit
         if (lane == 0)
             for (uint32_t k = (g > (uint32_t)kSlots ? g - kSlots : 0); k < g; ++k)
@@ -300,8 +316,13 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     }
 
     // ================= compute warps =================
-    // Inputs that do not depend on the previous kernel are requested before
-    // waiting for it: this CTA's router row and the RMSNorm gain.
+    uint32_t g = 0;
+    for (int l = 0; l < a.n_layers; ++l) {
+    const LW W = layer_w(a, l);
+    const uint16_t *xin = l == 0 ? a.x : (((l - 1) & 1) ? a.act1 : a.act0);
+    uint16_t *yout = l == a.n_layers - 1 ? a.y : ((l & 1) ? a.act1 : a.act0);
+    // Inputs that do not depend on the previous kernel (layer) are requested
+    // before waiting for it: this CTA's router row and the RMSNorm gain.
     uint4 rw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     uint4 gv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     const bool has_row = kRoute && (int)blockIdx.x < E;
@@ -309,13 +330,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     for (int q = 0; q < 2; ++q) {
         const int d8 = (tid + q * kCompute) * 8;
         if (d8 < D) {
-            if (has_row) rw[q] = ld_stream16(a.router_w + (size_t)blockIdx.x * D + d8);
-            if (a.gain) gv[q] = *reinterpret_cast<const uint4 *>(a.gain + d8);
+            if (has_row) rw[q] = ld_stream16(W.router_w + (size_t)blockIdx.x * D + d8);
+            if (W.gain) gv[q] = *reinterpret_cast<const uint4 *>(W.gain + d8);
         }
     }
 
-    pdl_wait();
-    pdl_launch_dependents();
+    if (l == 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+    } else {
+        grid_sync(a.gctr, a.status);     // every CTA's rows of the previous layer's output are written
+    }
 
     // ids and weights given by the caller (FFN-only variant): requested now,
     // consumed after the normalisation
@@ -332,7 +357,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     for (int q = 0; q < 2; ++q) {
         const int d8 = (tid + q * kCompute) * 8;
         if (d8 < D) {
-            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.x + d8));
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(xin + d8));
             *reinterpret_cast<uint4 *>(xraw + d8) = v;
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -346,7 +371,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         }
     }
     bar_compute();   // xraw complete before threads read each other's elements
-    if (a.gain) {
+    if (W.gain) {
         // the reduction order of block_rms_inv: stride-256 scalar partials,
         // a warp tree, then the 8 warp sums in order
         float ss = 0.f;
@@ -461,9 +486,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         }
         if (tid < K) {
             wsel[tid] = expf(lsel[tid] - m) / denom;
-            if (blockIdx.x == 0) {
-                a.idx_out[tid] = isel[tid];
-                a.w_out[tid] = wsel[tid];
+            if (blockIdx.x == 0 && a.idx_out) {
+                a.idx_out[l * K + tid] = isel[tid];
+                a.w_out[l * K + tid] = wsel[tid];
             }
         }
     } else {
@@ -493,7 +518,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     // Warp w takes pass pw = w % NCP (chunks pw*64 + lane and pw*64 + 32 + lane
     // of every row, so its 64 activations stay in registers) and row slot
     // w / NCP of each item; the NCP partial sums of a row meet in shared memory.
-    uint32_t g = 0;
     {
         const int NG = D / kGroup;
         const int pw = warp % NCP, rs = warp / NCP, rstep = kWarpsC / NCP;
@@ -566,12 +590,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
     for (int k = 0; k < 8; ++k) hq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float Hc = 0.f;
 
-    // Pass 0 runs the down-row code once on whatever the first ring slot
-    // holds and keeps nothing: a warp that is done with gate/up fetches those
-    // instructions while it would otherwise wait at the barrier.  Pass 1 is
-    // the real one.
+    // Pass 0 (first layer of a launch) runs the down-row code once on whatever
+    // the first ring slot holds and keeps nothing: a warp that is done with
+    // gate/up fetches those instructions while it would otherwise wait at the
+    // barrier.  Pass 1 is the real one.
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = l == 0 ? 0 : 1; pass < 2; ++pass) {
         const bool real = pass == 1;
         if (real) {
             bar_compute();
@@ -594,7 +618,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 mb_expect(&h_ready, hbytes);
                 bulk_g2s(hs, a.h, hbytes, &h_ready);
             }
-            warp_wait(&h_ready, 0, a.status);
+            warp_wait(&h_ready, l & 1, a.status);
             const float4 *hv = reinterpret_cast<const float4 *>(hs) + ((di * MC + (dc >> 3)) * 8) * 8 + (dc & 7);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -649,8 +673,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             y = fmaf(wsel[i], o, y);
             if (a.expert_out) a.expert_out[(size_t)i * D + d0 + r] = o;
         }
-        a.y[d0 + r] = f32_to_bf16(y);
+        yout[d0 + r] = f32_to_bf16(y);
     }
+    }   // layers
 }
 
 }  // namespace

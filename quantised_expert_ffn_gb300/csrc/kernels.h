@@ -71,6 +71,9 @@ struct DecodeArgs {
     float *h;                   // [K][F] fp32 scratch
     uint16_t *y;                // [D] bf16 out (may alias x)
     float *expert_out;          // [K][D] or NULL
+    const smoe_layer *layers;   // stack variant: device table of n_layers layers (NULL: the pointers above)
+    int n_layers;               // layers run by one launch (1 unless `layers` is set)
+    uint16_t *act0, *act1;      // stack variant: [D] bf16 activations between layers (ping-pong)
     int32_t *status;
 };
 cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t s, bool pdl);
@@ -95,6 +98,9 @@ struct FusedArgs {
     const int32_t *idx_in;      // [K] (FFN-only variant)
     const float *w_in;          // [K]
     float *expert_out;          // [K][D] or NULL
+    const smoe_layer *layers;   // stack variant: device table of n_layers layers (NULL: the pointers above)
+    int n_layers;               // layers run by one launch (1 unless `layers` is set)
+    uint16_t *act0, *act1;      // stack variant: [D] bf16 activations between layers (ping-pong)
     // plan (fused_plan)
     int grid, r_gu, dn_nr, dn_gran, dn_rs, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
 };

@@ -73,6 +73,7 @@ def _load():
         "smoe_moe_prefill_chunk": (I, [LP, P, I, P, P, P, P, Z, P]),
         "smoe_status_string": (ctypes.c_char_p, [I]),
         "smoe_moe_decode_noalloc": (I, [LP, P, P, P, P, P]),
+        "smoe_moe_decode_layers": (I, [LP, P, I, P, P, P, P, P, Z, P]),
         "smoe_last_cuda_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -86,7 +87,7 @@ _lib = _load()
 EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_status",
             "smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_ffn_decode",
             "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc",
-            "smoe_last_cuda_error")
+            "smoe_last_cuda_error", "smoe_moe_decode_layers")
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -199,3 +200,24 @@ def smoe_moe_decode_noalloc(layer: Layer, x, y, idx_out=None, w_out=None, stream
     serving loops or plug-ins whose host owns the device memory); see include/smoe.h."""
     _check(_lib.smoe_moe_decode_noalloc(layer.ref, _p(x), _p(y), _p(idx_out), _p(w_out),
                                         _stream(stream)), "smoe_moe_decode_noalloc")
+
+
+class LayerTable:
+    """Host array of smoe_layer structs for a list of Layer objects, and its
+    device copy (what smoe_moe_decode_layers reads on the GPU)."""
+
+    def __init__(self, layers, device="cuda"):
+        self.layers = list(layers)
+        n = len(self.layers)
+        self.host = (smoe_layer * n)(*[L.s for L in self.layers])
+        raw = bytes(memoryview(self.host).cast("B"))
+        self.dev = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
+        self.n = n
+
+
+def smoe_moe_decode_layers(table: LayerTable, x, y, idx_out=None, w_out=None, ws=None, stream=None):
+    """One decode token through every layer of `table` in one kernel launch."""
+    _check(_lib.smoe_moe_decode_layers(ctypes.cast(table.host, ctypes.POINTER(smoe_layer)), _p(table.dev),
+                                       int(table.n), _p(x), _p(y), _p(idx_out), _p(w_out), _p(ws),
+                                       0 if ws is None else ws.numel(), _stream(stream)),
+           "smoe_moe_decode_layers")

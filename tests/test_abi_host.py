@@ -104,6 +104,35 @@ def test_entry_points_reject_bad_arguments_on_host(lib):
     assert so.smoe_moe_decode(ctypes.byref(mis), P(4096), P(8192), None, None, None, ws, n, None) == lib.SMOE_ERR_INVALID_ARG
 
 
+def test_decode_layers_rejects_bad_arguments_on_host(lib):
+    so = lib._lib
+    P = ctypes.c_void_p
+    arr = (lib.smoe_layer * 3)(_layer(lib), _layer(lib), _layer(lib))
+    LP = ctypes.POINTER(lib.smoe_layer)
+    host = ctypes.cast(arr, LP)
+    ws = ctypes.c_void_p(1 << 24)
+    n = so.smoe_workspace_bytes(ctypes.byref(arr[0]), 1)
+    dev_tab = P(1 << 22)
+    call = lambda h, d, nl, x=P(4096), y=P(8192), i=None, w=None, wsp=ws, nb=n: \
+        so.smoe_moe_decode_layers(h, d, nl, x, y, i, w, wsp, nb, None)
+    assert call(host, dev_tab, 0) == lib.SMOE_ERR_INVALID_ARG            # no layers
+    assert call(None, dev_tab, 3) == lib.SMOE_ERR_INVALID_ARG            # no host table
+    assert call(host, None, 3) == lib.SMOE_ERR_INVALID_ARG               # no device table
+    assert call(host, P((1 << 22) + 4), 3) == lib.SMOE_ERR_INVALID_ARG   # misaligned device table
+    assert call(host, dev_tab, 3, x=P(4098)) == lib.SMOE_ERR_INVALID_ARG
+    assert call(host, dev_tab, 3, i=P(64)) == lib.SMOE_ERR_INVALID_ARG   # ids without weights
+    assert call(host, dev_tab, 3, wsp=None) == lib.SMOE_ERR_WORKSPACE
+    assert call(host, dev_tab, 3, nb=16) == lib.SMOE_ERR_WORKSPACE
+    arr[2].ffn_dim = 1536                                                 # layers of different shapes
+    assert call(host, dev_tab, 3) == lib.SMOE_ERR_INVALID_ARG
+    arr[2].ffn_dim = 768
+    arr[1].rms_gain = 1 << 20                                             # gain on one layer only
+    assert call(host, dev_tab, 3) == lib.SMOE_ERR_INVALID_ARG
+    arr[1].rms_gain = None
+    arr[1].d_model = 2000                                                 # unsupported layer
+    assert call(host, dev_tab, 3) == lib.SMOE_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
     for code in range(-6, 1):
         assert lib.smoe_status_string(code).startswith("SMOE_")

@@ -58,6 +58,10 @@ def layer(name, norm, seed=1337, ntp=True):
     return _cache[key]
 
 
+def bits_t(t):
+    return t.view(torch.int16)
+
+
 def dev(a):
     if a.dtype == np.uint16:
         return from_bits(a).cuda()
@@ -232,6 +236,73 @@ def test_moe_ffn_decode_given_ids(smoe, orc, name, ids):
     assert max_row_rel_l2(host(eo), o) <= TOL
     y_ref = bf16_f64(x) + (w.astype(np.float64)[:, None] * o).sum(0)
     assert rel_l2(bf16_f64(host(y)), y_ref) <= TOL
+    assert smoe.smoe_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("name,n", [("30b", 4), ("235b", 2), ("f1536", 3), ("f512", 3)])
+def test_decode_layers_equals_chained_layers(smoe, name, n):
+    """The one-launch stack gives, bit for bit, what n chained decode calls give
+    (outputs and every layer's ids and weights)."""
+    D, E, K, F = SHAPES[name]
+    Ws = [synth.layer_weights(D, E, F, K, seed=900 + i, device="cuda", rms_norm=True) for i in range(n)]
+    Ls = [smoe.Layer(W) for W in Ws]
+    table = smoe.LayerTable(Ls)
+    ws = smoe.workspace(Ls[0], 1)
+    x = synth.hidden(2, D, seed=12, device="cuda")
+    for t in range(2):
+        y = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+        idx = torch.empty((n, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((n, K), dtype=torch.float32, device="cuda")
+        smoe.smoe_moe_decode_layers(table, x[t], y, idx, w, ws)
+        cur = x[t].clone()
+        for i, L in enumerate(Ls):
+            nxt = torch.empty_like(cur)
+            ii = torch.empty(K, dtype=torch.int32, device="cuda")
+            wi = torch.empty(K, dtype=torch.float32, device="cuda")
+            smoe.smoe_moe_decode(L, cur, nxt, ii, wi, ws=ws)
+            assert torch.equal(ii, idx[i]) and torch.equal(wi, w[i]), i
+            cur = nxt
+        torch.cuda.synchronize()
+        assert torch.equal(bits_t(y), bits_t(cur))
+    assert smoe.smoe_read_device_status(ws) == 0
+
+
+def test_decode_layers_against_oracle(smoe, orc):
+    """Two 30B-shaped layers in one launch against the oracle chain, on tokens
+    whose routing margins hold at both layers."""
+    D, E, K, F = SHAPES["30b"]
+    Ws = [synth.layer_weights(D, E, F, K, seed=950 + i, device="cuda", rms_norm=True) for i in range(2)]
+    OLs = [oracle_layer(W) for W in Ws]
+    Ls = [smoe.Layer(W) for W in Ws]
+    table = smoe.LayerTable(Ls)
+    ws = smoe.workspace(Ls[0], 1)
+    Wabs = [np.abs(bf16_f64(OL.router_w)) for OL in OLs]
+    kept = 0
+    for attempt in range(40):
+        x = bits(synth.hidden(1, D, seed=5000 + attempt))[0]
+        refs, cur, ok = [], x, True
+        for OL, Wa in zip(OLs, Wabs):
+            r = orc.moe_token(OL, cur)
+            tau = 64 * 2.0 ** -24 * float((Wa @ np.abs(bf16_f64(r["xn"]))).max())
+            top = np.sort(r["logits"])[::-1][:K + 1]
+            ok = ok and bool(np.all(top[:-1] - top[1:] >= 10 * tau))
+            refs.append(r)
+            cur = r["y_bf16"]
+        if not ok:
+            continue
+        y = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+        idx = torch.empty((2, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((2, K), dtype=torch.float32, device="cuda")
+        smoe.smoe_moe_decode_layers(table, dev(x), y, idx, w, ws)
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert np.array_equal(host(idx)[i], refs[i]["idx"])
+            np.testing.assert_allclose(host(w)[i], refs[i]["w"], rtol=2e-5)
+        assert rel_l2(bf16_f64(host(y)), refs[1]["y"]) <= TOL
+        kept += 1
+        if kept == 2:
+            break
+    assert kept == 2
     assert smoe.smoe_read_device_status(ws) == 0
 
 
