@@ -120,7 +120,6 @@ __device__ __forceinline__ void grid_sync(unsigned long long *ctr, int32_t *stat
         if (v < target) {
             const uint64_t t0 = global_ns();
             while (true) {
-                __nanosleep(40);
                 asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
                 if (v >= target) break;
                 if (global_ns() - t0 > kWaitLimitNs) {
@@ -460,6 +459,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         if (tid < E) {
             int r0 = 0, r1 = 0;
             const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(keys);
+#pragma unroll 8
             for (int j = 0; j < E / 2; ++j) {
                 const ulonglong2 kk = k2[j];
                 r0 += kk.x > mykey;
@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             }
         }
         bar_compute();
+        if (tid == 0) mb_arrive(&idx_ready);   // ranked ids are all the producer needs
         const float m = lsel[0];
         float denom = 0.f;
         if (a.norm_topk_prob) {
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         }
     }
     bar_compute();
-    if (tid == 0) mb_arrive(&idx_ready);
+    if (!kRoute && tid == 0) mb_arrive(&idx_ready);
 
     // ---- phase 1: gate/up rows -> h, the activations in registers ----
     // Warp w takes pass pw = w % NCP (chunks pw*64 + lane and pw*64 + 32 + lane
