@@ -42,7 +42,7 @@ D235, F235, L235 = 4096, 1536, 94
 SEED = 1337
 PER_LAYER = False   # --per-layer: decode through one smoe_moe_decode call per layer
 
-# sources of the kernel the roofline reports (the fused decode layer, FFN-only variant)
+# sources of the kernel the roofline reports (the fused decode kernel)
 FFN_SOURCES = ["quantised_expert_ffn_gb300/csrc/decode_fused.cu",
                "quantised_expert_ffn_gb300/csrc/common.cuh",
                "quantised_expert_ffn_gb300/csrc/kernels.h"]
@@ -121,23 +121,27 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def traffic_from_profile(name, source_files):
-    """DRAM bytes per launch recorded in profiles/<name>.md, if the kernels it
+def traffic_from_profile(name, source_files, key="traffic_bytes_per_layer"):
+    """DRAM bytes recorded under `key` in profiles/<name>.md, if the kernels it
     was taken on are unchanged (sha256 of their sources matches)."""
     path = os.path.join(ROOT, "profiles", name + ".md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m = re.search(key + r":\s*([0-9.eE+]+)", txt)
     h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", txt)
     if not m or not h:
         return None
+    if not source_digest(source_files).startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+def source_digest(source_files):
     cur = hashlib.sha256()
     for f in source_files:
         cur.update(open(os.path.join(ROOT, f), "rb").read())
-    if not cur.hexdigest().startswith(h.group(1)):
-        return None
-    return float(m.group(1))
+    return cur.hexdigest()
 
 
 def replica_rate(units_per_rank, elapsed_ms, device=None):
