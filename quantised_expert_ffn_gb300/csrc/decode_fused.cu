@@ -150,6 +150,25 @@ __device__ __forceinline__ float dot32(uint4 c, const float4 (&x)[8]) {
     return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
+// Warp-wide sums of eight values at once (v[j] of every lane): 9 shuffles
+// instead of 40.  Each exchange halves the values a lane carries; lane L ends
+// with the total of v[4*b4 + 2*b3 + b2] (b = bits of L), held by 4 lanes.
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w[j] = (b4 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[j + 4], 16);
+    float u[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        u[j] = (b3 ? w[j + 2] : w[j]) + __shfl_xor_sync(0xffffffffu, b3 ? w[j] : w[j + 2], 8);
+    float t = (b2 ? u[1] : u[0]) + __shfl_xor_sync(0xffffffffu, b2 ? u[0] : u[1], 4);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    return t;
+}
+
 // ---------------------------------------------------------------- work lists
 
 // Gate/up: CTA c owns row pairs [P*c/G, P*(c+1)/G) of the P = K*F (slot, row)
@@ -531,6 +550,26 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             xb[q] = xs4[((pw * 2 + 1) * 8 + q) * 32 + lane];
         }
         const float Xa = xc[ca], Xb = xc[cbk];
+        // the lane partials of up to four rows wait in registers (newest first)
+        // and are summed together by warp_sum8
+        float acc8[8];
+        uint32_t trow = 0;          // byte k: 1 + row pair index of slot k (0 = empty)
+        auto reset = [&]() {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc8[q] = 0.f;
+            trow = 0;
+        };
+        auto flush = [&]() {
+            const float tot = warp_sum8(acc8, lane);
+            if ((lane & 3) == 0) {
+                const int j = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                const int t = (int)((trow >> (8 * (j >> 1))) & 0xFFu) - 1;
+                if (t >= 0) part[(t * NCP + pw) * 2 + (j & 1)] = tot;
+            }
+            reset();
+        };
+        reset();
+        int nacc = 0;
         for (int p = p0; p < p1; ++g) {
             const int i = p / F, j0 = p - i * F, n = min(a.r_gu, min(p1 - p, F - j0));
             const uint32_t s = g % kSlots;
@@ -561,18 +600,21 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                     ag += s0 * A + (b0 - 128.f * s0) * Xb;
                     au += s1 * B + (b1 - 128.f * s1) * Xb;
                 }
-                ag = warp_sum(ag);
-                au = warp_sum(au);
-                if (lane == 0) {
-                    const int t = p + r - p0;                 // row pair index within this CTA
-                    part[(t * NCP + pw) * 2] = ag;
-                    part[(t * NCP + pw) * 2 + 1] = au;
+#pragma unroll
+                for (int q = 7; q >= 2; --q) acc8[q] = acc8[q - 2];
+                acc8[0] = ag;
+                acc8[1] = au;
+                trow = (trow << 8) | (uint32_t)(p + r - p0 + 1);   // row pair index within this CTA
+                if (++nacc == 4) {
+                    flush();
+                    nacc = 0;
                 }
             }
             __syncwarp();
             if (lane == 0) mb_arrive(&empty[s]);
             p += n;
         }
+        if (nacc > 0) flush();
     }
 
     // ---- phase 2 set-up: down rows of this CTA ----
