@@ -67,6 +67,7 @@ struct TcParams {
     int out_ld;             // row length of the output (F for h, D for o)
     const int32_t *n_union, *union_ids, *offsets;
     const uint16_t *s0, *b0, *s1, *b1;   // scales/biases of A0 (gate or down) and A1 (up)
+    int vec_scales;         // K/64 % 8 == 0 and 16-byte aligned scale arrays: 8 groups per load
     __half *hout;           // gate/up: h [slots][F] fp16, K-permuted
     float *oout;            // down: o [slots][D] fp32
     int32_t *status;
@@ -187,6 +188,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // ---- dequant ---------------------------------------------------------------
+
+// bf16 element j (runtime, 0..7) of 8 packed in a uint4, as a half2 pair.
+__device__ __forceinline__ __half2 pick_h2(const uint4 &v, int j) {
+    const uint32_t w = (j & 4) ? ((j & 2) ? v.w : v.z) : ((j & 2) ? v.y : v.x);
+    const uint16_t b = (j & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xFFFFu);
+    return __half2half2(__float2half_rn(bf16_to_f32(b)));
+}
 
 // 8 codes of one word -> 4 half2 (e_i, e_{i+4}), each s*q + b with one rounding.
 __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
@@ -360,16 +368,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int e = p.union_ids[u];
             const size_t row = (size_t)e * p.rows_per_expert + tile * kTile + r;
             const int NG = p.k_dim / kGroup;
+            // Scales and biases of this row: with vec_scales, 8 groups per 16-byte
+            // load, the next 8 requested one block ahead of use.
+            uint4 vs0{}, vb0{}, vs1{}, vb1{}, ns0{}, nb0{}, ns1{}, nb1{};
+            auto load8 = [&](int c8, uint4 &ts0, uint4 &tb0, uint4 &ts1, uint4 &tb1) {
+                const size_t o = row * NG + c8;
+                ts0 = __ldg(reinterpret_cast<const uint4 *>(p.s0 + o));
+                tb0 = __ldg(reinterpret_cast<const uint4 *>(p.b0 + o));
+                if (kPair) {
+                    ts1 = __ldg(reinterpret_cast<const uint4 *>(p.s1 + o));
+                    tb1 = __ldg(reinterpret_cast<const uint4 *>(p.b1 + o));
+                }
+            };
+            if (p.vec_scales) {
+                load8(0, vs0, vb0, vs1, vb1);
+                if (NC > 8) load8(8, ns0, nb0, ns1, nb1);
+            }
             bool ok = true;
             for (int c = 0; c < NC; ++c, ++g) {
                 const int s = g % kStages, a = g % kAStages;
-                // scales/biases of this row and group (L1-cached: 16 groups share a sector)
-                const __half2 s0 = __half2half2(__float2half_rn(bf16_to_f32(p.s0[row * NG + c])));
-                const __half2 b0 = __half2half2(__float2half_rn(bf16_to_f32(p.b0[row * NG + c])));
-                __half2 s1 = s0, b1 = b0;
-                if (kPair) {
-                    s1 = __half2half2(__float2half_rn(bf16_to_f32(p.s1[row * NG + c])));
-                    b1 = __half2half2(__float2half_rn(bf16_to_f32(p.b1[row * NG + c])));
+                __half2 s0, b0, s1, b1;
+                if (p.vec_scales) {
+                    if ((c & 7) == 0 && c > 0) {
+                        vs0 = ns0; vb0 = nb0; vs1 = ns1; vb1 = nb1;
+                        if (c + 8 < NC) load8(c + 8, ns0, nb0, ns1, nb1);
+                    }
+                    s0 = pick_h2(vs0, c & 7);
+                    b0 = pick_h2(vb0, c & 7);
+                    s1 = s0, b1 = b0;
+                    if (kPair) {
+                        s1 = pick_h2(vs1, c & 7);
+                        b1 = pick_h2(vb1, c & 7);
+                    }
+                } else {
+                    // scales/biases of this row and group (L1-cached: 16 groups share a sector)
+                    s0 = __half2half2(__float2half_rn(bf16_to_f32(p.s0[row * NG + c])));
+                    b0 = __half2half2(__float2half_rn(bf16_to_f32(p.b0[row * NG + c])));
+                    s1 = s0, b1 = b0;
+                    if (kPair) {
+                        s1 = __half2half2(__float2half_rn(bf16_to_f32(p.s1[row * NG + c])));
+                        b1 = __half2half2(__float2half_rn(bf16_to_f32(p.b1[row * NG + c])));
+                    }
                 }
                 if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
                 const unsigned char *stg = st_ring + s * S::kStageBytes;
@@ -561,6 +600,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     gu.union_ids = a.union_ids;
     gu.offsets = a.offsets;
     gu.s0 = a.gs; gu.b0 = a.gb; gu.s1 = a.us; gu.b1 = a.ub;
+    auto a16 = [](const void *q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    gu.vec_scales = (a.D / kGroup) % 8 == 0 && a16(a.gs) && a16(a.gb) && a16(a.us) && a16(a.ub);
     gu.hout = a.hbuf;
     gu.status = a.status;
     if ((e = launch_tc<true>(mg, mu, mx, gu, s, grid)) != cudaSuccess) return e;
@@ -571,6 +612,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     dn.k_dim = a.F;
     dn.out_ld = a.D;
     dn.s0 = a.ds; dn.b0 = a.db; dn.s1 = nullptr; dn.b1 = nullptr;
+    dn.vec_scales = (a.F / kGroup) % 8 == 0 && a16(a.ds) && a16(a.db);
     dn.hout = nullptr;
     dn.oout = a.obuf;
     return launch_tc<false>(md, md, mh, dn, s, grid);
