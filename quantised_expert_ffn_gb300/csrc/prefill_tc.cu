@@ -12,21 +12,27 @@
 //
 // One persistent CTA per SM walks a static list of units (union expert u,
 // 128-row tile); per unit the K dimension is consumed in chunks of 64 (one Q4
-// group, one 128-byte swizzle atom).  Warp roles:
+// group).  Warp roles:
 //   warps 0-7   dequant: read the TMA-staged codes of a chunk from shared
 //               memory, turn them into fp16 w = s*q + b (one rounding; exact
-//               when b = -8 s, since s*(q-8) needs at most 11 bits) and
-//               write the A tile in the 128-byte-swizzled K-major layout;
+//               when b = -8 s, since s*(q-8) needs at most 11 bits) and store
+//               them straight into tensor memory (tcgen05.st): warp w owns
+//               TMEM lanes 32*(w%4).. = tile rows, and K half w/4 of each chunk;
 //   warp 12     TMA: codes tiles (no swizzle) and the bucket's activation
-//               tile (128-byte swizzle) into a ring of stages;
-//   warp 13     MMA: one thread issues tcgen05.mma (M=128, N=pad16(bucket),
-//               K=16, fp16 x fp16 -> fp32 in TMEM) and commits stages back;
+//               tile (128-byte swizzle) into a ring of shared-memory stages;
+//   warp 13     MMA: one thread issues tcgen05.mma with A from tensor memory
+//               (M=128 weight rows, K=16) and B from shared memory (N =
+//               pad16(bucket) tokens), fp16 x fp16 -> fp32 in TMEM, and commits
+//               stages back;
 //   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
-// Two TMEM accumulator buffers let the epilogue of one unit overlap the main
-// loop of the next.  Every wait on an mbarrier is bounded: on timeout the CTA
-// records SMOE_ERR_TIMEOUT, all roles drain and the TMEM is freed.
+// TMEM: columns 0-255 two accumulator buffers (gate, up: 64 columns each), so
+// the epilogue of one unit overlaps the main loop of the next; columns
+// 256-511 four stages of dequantised A.  Keeping A out of shared memory leaves
+// shared-memory bandwidth to the TMA and to the B operand.  Every wait on an
+// mbarrier is bounded: on timeout the CTA records SMOE_ERR_TIMEOUT, all roles
+// drain and the TMEM is freed.
 //
 // The dequant writes the 8 elements of each 32-bit code word as the pairs
 // (e0,e4),(e1,e5),(e2,e6),(e3,e7) -- the order the fp16 magic-number unpack
@@ -50,13 +56,14 @@ constexpr int kMmaWarp = 13;
 constexpr int kTile = 128;
 constexpr int kKc = 64;
 constexpr int kNmax = 64;
-constexpr int kStages = 6;
-constexpr int kAStages = 3;
+constexpr int kStages = 8;
+constexpr int kAStages = 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccStride = 256;
-constexpr uint32_t kUpCol = 128;
+constexpr uint32_t kAccStride = 128;                  // two accumulator buffers: columns 0-127, 128-255
+constexpr uint32_t kUpCol = 64;                       // up accumulator after gate's (N <= 64 columns each)
+constexpr uint32_t kACol0 = 256;                      // A stages: columns 256-511
+constexpr uint32_t kACols = 32;                       // one matrix's 128 x 64 fp16 chunk: 32 columns
 constexpr int kCodeBytes = kTile * kKc / 2;          // 4 KB of codes per matrix per stage
-constexpr int kATileBytes = kTile * kKc * 2;         // 16 KB fp16 A tile
 constexpr int kBTileBytes = kNmax * kKc * 2;         // 8 KB fp16 B tile (up to 64 rows)
 
 struct TcParams {
@@ -107,12 +114,13 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
 
 // Wait for the phase of `parity` to complete, bounded in wall time; false on
 // timeout (which also raises the CTA's abort flag) or when another role aborted.
+// Plain try_wait polling: a long suspend hint wakes the waiter late.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag,
                                           int32_t *status) {
     if (mbar_try(b, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_suspend(smem_u32(b), parity, kSuspendHintNs)) return true;
+        if (mbar_try(b, parity)) return true;
         if (*abort_flag) return false;
         if (global_ns() - t0 > kWaitLimitNs) break;
     }
@@ -130,9 +138,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -165,6 +170,28 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// A operand from tensor memory: lane m holds row m, two fp16 K elements per column.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.u32 p, %4, 0;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[4][4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+        " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0][0]), "r"(r[0][1]), "r"(r[0][2]), "r"(r[0][3]), "r"(r[1][0]), "r"(r[1][1]), "r"(r[1][2]),
+        "r"(r[1][3]), "r"(r[2][0]), "r"(r[2][1]), "r"(r[2][2]), "r"(r[2][3]), "r"(r[3][0]), "r"(r[3][1]),
+        "r"(r[3][2]), "r"(r[3][3])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
@@ -218,8 +245,7 @@ template <bool kPair>
 struct Smem {
     static constexpr int kMats = kPair ? 2 : 1;
     static constexpr int kStageBytes = kMats * kCodeBytes + kBTileBytes;
-    static constexpr int kAOff = 0;
-    static constexpr int kStageOff = kAStages * kMats * kATileBytes;
+    static constexpr int kStageOff = 0;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
     static constexpr int kBytes = kBarOff + 1024;   // barriers + tmem slot + flags
 };
@@ -235,7 +261,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // 1024-byte alignment for the swizzled tiles
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *a_ring = sm + S::kAOff;
     unsigned char *st_ring = sm + S::kStageOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
     uint64_t *full = bars;                    // [kStages]
@@ -337,15 +362,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after();
                     issued = true;
-                    const uint32_t abase = smem_u32(a_ring + a * S::kMats * kATileBytes);
+                    const uint32_t acol = tmem + kACol0 + a * S::kMats * kACols;
                     const uint32_t bbase = smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes);
 #pragma unroll
                     for (int kk = 0; kk < kKc / 16; ++kk) {
                         const uint64_t bd = smem_desc_sw128(bbase + kk * 32);
                         const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-                        mma_f16(d0, smem_desc_sw128(abase + kk * 32), bd, idesc, acc);
-                        if (kPair)
-                            mma_f16(d0 + kUpCol, smem_desc_sw128(abase + kATileBytes + kk * 32), bd, idesc, acc);
+                        mma_f16_ta(d0, acol + kk * 8, bd, idesc, acc);
+                        if (kPair) mma_f16_ta(d0 + kUpCol, acol + kACols + kk * 8, bd, idesc, acc);
                     }
                     mma_commit(&aempty[a]);
                     mma_commit(&empty[s]);
@@ -361,7 +385,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp < 8) {
         // ---------------- dequant producers ----------------
-        const int r = tid >> 1, h = tid & 1;          // weight row in the tile, half of the chunk
+        // warp w writes TMEM lanes 32*(w%4).. (its quarter): row r of the tile,
+        // K half h of each chunk (columns 16h..16h+15 of the matrix's 32)
+        const int r = 32 * (warp & 3) + lane, h = warp >> 2;
+        const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t g = 0;
         for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x) {
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
@@ -410,7 +437,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         b1 = __half2half2(__float2half_rn(bf16_to_f32(p.b1[row * NG + c])));
                     }
                 }
-                if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+                // waits are warp-uniform: the TMEM store below is warp-collective
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
                 const unsigned char *stg = st_ring + s * S::kStageBytes;
                 const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 32 + h * 16);
                 uint4 c1 = c0;
@@ -427,17 +458,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dequant_word(c1.z, s1, b1, q1[2]);
                     dequant_word(c1.w, s1, b1, q1[3]);
                 }
-                if (!mbar_wait(&aempty[a], ((g / kAStages) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-                unsigned char *at = a_ring + a * S::kMats * kATileBytes + r * 128;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int phys = ((4 * h + j) ^ (r & 7)) * 16;
-                    *reinterpret_cast<uint4 *>(at + phys) = make_uint4(q0[j][0], q0[j][1], q0[j][2], q0[j][3]);
-                    if (kPair)
-                        *reinterpret_cast<uint4 *>(at + kATileBytes + phys) =
-                            make_uint4(q1[j][0], q1[j][1], q1[j][2], q1[j][3]);
+                if (!__all_sync(0xffffffffu, mbar_wait(&aempty[a], ((g / kAStages) & 1) ^ 1, abort_flag, p.status))) {
+                    ok = false;
+                    break;
                 }
-                fence_proxy_async();
+                tc_fence_after();
+                const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols + h * 16;
+                tmem_st16(acol, q0);
+                if (kPair) tmem_st16(acol + kACols, q1);
+                tmem_wait_st();
+                tc_fence_before();
                 mbar_arrive(&afull[a]);
             }
             if (!ok) break;
