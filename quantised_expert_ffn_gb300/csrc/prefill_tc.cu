@@ -41,6 +41,8 @@
 // unchanged.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -586,7 +588,10 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
 template <bool kPair>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap (&b)[4],
                       const TcParams &p, cudaStream_t s, int grid) {
-    const size_t smem = Smem<kPair>::kBytes + 1024;
+    // More than half of an SM's shared memory: one CTA per SM.  Two resident
+    // CTAs would each want all 512 TMEM columns, and the second would wait in
+    // tcgen05.alloc until the first exits.
+    const size_t smem = std::max<size_t>(Smem<kPair>::kBytes + 1024, 120 * 1024);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
