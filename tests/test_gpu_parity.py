@@ -401,3 +401,83 @@ def test_alternate_engines_in_subprocess(smoe):
                         "tests/test_gpu_parity.py", "-k", "(prefill or decode) and not subprocess"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+# ------------------------------------------------------------- skewed routing
+
+def _margin_ok(orc, OL, x_row, Wabs, K, factor=10.0):
+    xn = orc.rmsnorm(OL, x_row)
+    lg = orc.router_logits(OL, xn)
+    tau = 64 * 2.0 ** -24 * float((Wabs @ np.abs(bf16_f64(xn))).max())
+    top = np.sort(lg)[::-1][:K + 1]
+    return bool(np.all(top[:-1] - top[1:] >= factor * tau)), lg
+
+
+def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
+    """Zipf(1.2)-biased router logits (x_t = z_t + pinv(Wr) b): a 64-token
+    chunk whose largest bucket holds 30-60 tokens (at least 4x the mean bucket),
+    through the prefill path; then a decode stream whose consecutive tokens share about
+    46% of their experts, through the decode path -- both against the oracle."""
+    W, OL = layer("30b", True)
+    D, E, K = W.d_model, W.n_experts, W.top_k
+    Wabs = np.abs(bf16_f64(OL.router_w))
+    L = smoe.Layer(W)
+    chosen = None
+    for scale in (1.0, 1.5, 2.0, 3.0, 4.0, 6.0):
+        cand = bits(synth.zipf_bias_hidden(256, W.router_w.float(), 1.2, scale, seed=31))
+        keep = []
+        for r in cand:
+            ok, lg = _margin_ok(orc, OL, r, Wabs, K)
+            if ok:
+                keep.append(r)
+            if len(keep) == 64:
+                break
+        if len(keep) < 64:
+            continue
+        x = np.stack(keep)
+        idx_ref = np.stack([orc.topk(orc.router_logits(OL, orc.rmsnorm(OL, r)), K) for r in x])
+        sizes = np.bincount(idx_ref.ravel(), minlength=E)
+        if 30 <= sizes.max() <= 60:
+            chosen = (scale, x, sizes)
+            break
+    assert chosen is not None, "no bias scale gave a 30-60 token bucket"
+    scale, x, sizes = chosen
+    assert sizes.max() >= 4 * sizes.mean()                 # skewed: the largest bucket far above the mean
+    ws = smoe.workspace(L, 64)
+    y = torch.empty((64, D), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((64, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((64, K), dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, dev(x), 64, y, idx, w, ws)
+    torch.cuda.synchronize()
+    assert smoe.smoe_read_device_status(ws) == 0
+    ref = orc.moe_tokens(OL, x)
+    assert np.array_equal(host(idx), ref["idx"])
+    np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
+    assert max_row_rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+
+    # decode stream with ~46% adjacent overlap (rho picked from a fixed list)
+    best = None
+    for rho in (0.5, 0.6, 0.7, 0.75, 0.8, 0.85, 0.9):
+        s = bits(synth.overlap_stream(24, D, rho, seed=47))
+        ids = [set(orc.topk(orc.router_logits(OL, orc.rmsnorm(OL, r)), K).tolist()) for r in s]
+        ov = np.mean([len(a & b) / K for a, b in zip(ids[:-1], ids[1:])])
+        if best is None or abs(ov - 0.46) < abs(best[1] - 0.46):
+            best = (rho, ov, s)
+    rho, ov, stream = best
+    assert 0.3 <= ov <= 0.6, ov
+    ws1 = smoe.workspace(L, 1)
+    checked = 0
+    for r in stream:
+        ok, _ = _margin_ok(orc, OL, r, Wabs, K)
+        if not ok:
+            continue
+        yd = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+        ii = torch.empty(K, dtype=torch.int32, device="cuda")
+        smoe.smoe_moe_decode(L, dev(r), yd, ii, None, None, ws1)
+        torch.cuda.synchronize()
+        rr = orc.moe_token(OL, r)
+        assert np.array_equal(host(ii), rr["idx"])
+        assert rel_l2(bf16_f64(host(yd)), rr["y"]) <= TOL
+        checked += 1
+    assert checked >= 8
+    assert smoe.smoe_read_device_status(ws1) == 0
