@@ -58,8 +58,11 @@ constexpr int kMmaWarp = 13;
 constexpr int kTile = 128;
 constexpr int kKc = 64;
 constexpr int kNmax = 64;
-constexpr int kStages = 8;
-constexpr int kAStages = 4;
+// One ring of kStages stages: shared memory holds a stage's codes and
+// activation tile, TMEM columns from kACol0 its dequantised A.  A stage is
+// refilled only after the MMA that read it has completed (the TMA waits for
+// it), so a producer that sees the stage's codes land may overwrite its A.
+constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 128;                  // two accumulator buffers: columns 0-127, 128-255
 constexpr uint32_t kUpCol = 64;                       // up accumulator after gate's (N <= 64 columns each)
@@ -265,11 +268,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *st_ring = sm + S::kStageOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
-    uint64_t *full = bars;                    // [kStages]
-    uint64_t *empty = full + kStages;         // [kStages]
-    uint64_t *afull = empty + kStages;        // [kAStages]
-    uint64_t *aempty = afull + kAStages;      // [kAStages]
-    uint64_t *accfull = aempty + kAStages;    // [2]
+    uint64_t *full = bars;                    // [kStages] codes + activations landed
+    uint64_t *empty = full + kStages;         // [kStages] codes read and the stage's MMAs complete
+    uint64_t *afull = empty + kStages;        // [kStages] dequantised A written
+    uint64_t *accfull = afull + kStages;      // [2]
     uint64_t *accempty = accfull + 2;         // [2]
     uint64_t *drain = accempty + 2;           // [1] all issued MMAs complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -282,10 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kProdThreads + 1);
         }
-        for (int i = 0; i < kAStages; ++i) {
-            mbar_init(&afull[i], kProdThreads);
-            mbar_init(&aempty[i], 1);
-        }
+        for (int i = 0; i < kStages; ++i) mbar_init(&afull[i], kProdThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accfull[i], 1);
             mbar_init(&accempty[i], 128);
@@ -356,8 +355,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t d0 = tmem + b * kAccStride;
                 bool ok = true;
                 for (int c = 0; c < NC; ++c, ++g) {
-                    const int s = g % kStages, a = g % kAStages;
-                    if (!mbar_wait(&afull[a], (g / kAStages) & 1, abort_flag, p.status) ||
+                    const int s = g % kStages, a = s;
+                    if (!mbar_wait(&afull[a], (g / kStages) & 1, abort_flag, p.status) ||
                         !mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -373,7 +372,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mma_f16_ta(d0, acol + kk * 8, bd, idesc, acc);
                         if (kPair) mma_f16_ta(d0 + kUpCol, acol + kACols + kk * 8, bd, idesc, acc);
                     }
-                    mma_commit(&aempty[a]);
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
@@ -415,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             bool ok = true;
             for (int c = 0; c < NC; ++c, ++g) {
-                const int s = g % kStages, a = g % kAStages;
+                const int s = g % kStages, a = s;
                 __half2 s0, b0, s1, b1;
                 if (p.vec_scales) {
                     if ((c & 7) == 0 && c > 0) {
@@ -460,11 +458,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dequant_word(c1.z, s1, b1, q1[2]);
                     dequant_word(c1.w, s1, b1, q1[3]);
                 }
-                if (!__all_sync(0xffffffffu, mbar_wait(&aempty[a], ((g / kAStages) & 1) ^ 1, abort_flag, p.status))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                tc_fence_after();      // A stage a: its last MMAs completed before these codes landed
                 const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols + h * 16;
                 tmem_st16(acol, q0);
                 if (kPair) tmem_st16(acol + kACols, q1);
