@@ -167,22 +167,22 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
+// A operand from tensor memory: lane m holds row m, two fp16 K elements per
+// column.  The MMAs of one K chunk (64 = 4 x 16) for one A matrix in a single block:
+// A columns a, a+8, a+16, a+24 of TMEM; B descriptors b0 + 2*kk (32 bytes
+// apart); the first MMA accumulates only when `acc` is set.
+__device__ __forceinline__ void mma_chunk_ta(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
+                                             uint32_t acc) {
     asm volatile(
-        "{ .reg .pred p; setp.ne.u32 p, %4, 0;"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// A operand from tensor memory: lane m holds row m, two fp16 K elements per column.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.u32 p, %4, 0;"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        "{ .reg .pred p, t; .reg .b64 b1, b2, b3; .reg .b32 a1, a2, a3;"
+        " setp.ne.u32 p, %4, 0; setp.eq.u32 t, %4, %4;"
+        " add.s64 b1, %2, 2; add.s64 b2, %2, 4; add.s64 b3, %2, 6;"
+        " add.s32 a1, %1, 8; add.s32 a2, %1, 16; add.s32 a3, %1, 24;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t; }" ::"r"(d),
+        "r"(a), "l"(b0), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -364,14 +364,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after();
                     issued = true;
                     const uint32_t acol = tmem + kACol0 + a * S::kMats * kACols;
-                    const uint32_t bbase = smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kKc / 16; ++kk) {
-                        const uint64_t bd = smem_desc_sw128(bbase + kk * 32);
-                        const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-                        mma_f16_ta(d0, acol + kk * 8, bd, idesc, acc);
-                        if (kPair) mma_f16_ta(d0 + kUpCol, acol + kACols + kk * 8, bd, idesc, acc);
-                    }
+                    const uint64_t bd = smem_desc_sw128(smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes));
+                    const uint32_t acc = c > 0 ? 1u : 0u;
+                    mma_chunk_ta(d0, acol, bd, idesc, acc);
+                    if (kPair) mma_chunk_ta(d0 + kUpCol, acol + kACols, bd, idesc, acc);
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
