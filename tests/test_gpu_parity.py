@@ -43,6 +43,11 @@ SHAPES = {
     # (idle lanes in the gate/up sweep), F/32 = 12 and 4 chunks per down row
     "f1536": (1536, 64, 6, 384),
     "f512": (512, 16, 4, 128),
+    # limits and degenerate cases: the largest layer the library takes (d_model 8192,
+    # 256 experts, top-16, k*F = 16384), every expert selected (k = E), one expert
+    "max": (8192, 256, 16, 1024),
+    "kall": (512, 8, 8, 128),
+    "one": (512, 1, 1, 128),
 }
 _cache = {}
 
@@ -481,3 +486,38 @@ def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
         checked += 1
     assert checked >= 8
     assert smoe.smoe_read_device_status(ws1) == 0
+
+
+@pytest.mark.parametrize("name", ["max", "kall", "one"])
+def test_limits_and_degenerate_layers(smoe, orc, name):
+    """Decode (one token) and a prefill chunk at the library's largest layer, with
+    every expert selected, and with a single expert -- against the oracle."""
+    W, OL = layer(name, True)
+    D, K = W.d_model, W.top_k
+    T = 4 if name == "max" else 16
+    x = margin_tokens(OL, T, seed=321)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, T)
+    # decode, token 0
+    y = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    w = torch.empty(K, dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_decode(L, dev(x[0]), y, idx, w, None, ws)
+    torch.cuda.synchronize()
+    ref = orc.moe_token(OL, x[0])
+    assert np.array_equal(host(idx), ref["idx"])
+    np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
+    assert rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+    if K == W.n_experts:
+        assert sorted(host(idx).tolist()) == list(range(K))      # k = E: every expert, once
+    if K == 1:
+        assert float(host(w)[0]) == 1.0
+    # prefill chunk
+    yc = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    ic = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, dev(x), T, yc, ic, None, ws)
+    torch.cuda.synchronize()
+    refc = orc.moe_tokens(OL, x)
+    assert np.array_equal(host(ic), refc["idx"])
+    assert max_row_rel_l2(bf16_f64(host(yc)), refc["y"]) <= TOL
+    assert smoe.smoe_read_device_status(ws) == 0
