@@ -244,7 +244,7 @@ def test_moe_ffn_decode_given_ids(smoe, orc, name, ids):
     assert smoe.smoe_read_device_status(ws) == 0
 
 
-@pytest.mark.parametrize("name,n", [("30b", 4), ("235b", 2), ("f1536", 3), ("f512", 3)])
+@pytest.mark.parametrize("name,n", [("30b", 4), ("235b", 2), ("f1536", 3), ("f512", 3), ("one", 3)])
 def test_decode_layers_equals_chained_layers(smoe, name, n):
     """The one-launch stack gives, bit for bit, what n chained decode calls give
     (outputs and every layer's ids and weights)."""
@@ -270,6 +270,60 @@ def test_decode_layers_equals_chained_layers(smoe, name, n):
         torch.cuda.synchronize()
         assert torch.equal(bits_t(y), bits_t(cur))
     assert smoe.smoe_read_device_status(ws) == 0
+
+
+def test_decode_layers_long_stack(smoe):
+    """A long stack (1,030 layers, three weight sets in turn) in one call
+    equals the chained single-layer calls bit for bit."""
+    D, E, K, F = SHAPES["f512"]
+    Ws = [synth.layer_weights(D, E, F, K, seed=970 + i, device="cuda", rms_norm=True) for i in range(3)]
+    base = [smoe.Layer(W) for W in Ws]
+    n = 1030
+    Ls = [base[i % 3] for i in range(n)]
+    table = smoe.LayerTable(Ls)
+    ws = smoe.workspace(base[0], 1)
+    x = synth.hidden(1, D, seed=13, device="cuda")[0]
+    y = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((n, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((n, K), dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_decode_layers(table, x, y, idx, w, ws)
+    cur = x.clone()
+    ii = torch.empty((n, K), dtype=torch.int32, device="cuda")
+    wi = torch.empty((n, K), dtype=torch.float32, device="cuda")
+    for i, L in enumerate(Ls):
+        nxt = torch.empty_like(cur)
+        smoe.smoe_moe_decode(L, cur, nxt, ii[i], wi[i], ws=ws)
+        cur = nxt
+    torch.cuda.synchronize()
+    assert torch.equal(ii, idx) and torch.equal(wi, w)
+    assert torch.equal(bits_t(y), bits_t(cur))
+    assert smoe.smoe_read_device_status(ws) == 0
+
+
+def test_one_workspace_across_shapes(smoe):
+    """One workspace serves stacks of different shapes in turn (the larger
+    shape, the smaller, the larger again); each result equals that of a fresh
+    workspace bit for bit."""
+    shapes = {}
+    for name, n in (("30b", 3), ("f512", 4)):
+        D, E, K, F = SHAPES[name]
+        Ls = [smoe.Layer(synth.layer_weights(D, E, F, K, seed=980 + i, device="cuda", rms_norm=True))
+              for i in range(n)]
+        shapes[name] = (Ls, smoe.LayerTable(Ls), synth.hidden(1, D, seed=14, device="cuda")[0])
+
+    def run(name, ws):
+        Ls, table, x = shapes[name]
+        y = torch.empty_like(x)
+        smoe.smoe_moe_decode_layers(table, x, y, None, None, ws)
+        torch.cuda.synchronize()
+        return y
+
+    shared = smoe.workspace(shapes["30b"][0][0], 1)
+    for name in ("30b", "f512", "30b", "f512", "30b"):
+        y = run(name, shared)
+        y_fresh = run(name, smoe.workspace(shapes[name][0][0], 1))
+        assert torch.equal(bits_t(y), bits_t(y_fresh)), name
+    assert smoe.smoe_read_device_status(shared) == 0
 
 
 def test_decode_layers_against_oracle(smoe, orc):
