@@ -271,3 +271,30 @@ def omp_threads() -> int:
     if v and v.isdigit():
         return int(v)
     return len(os.sched_getaffinity(0))
+
+
+def dense_matvec(w, x) -> np.ndarray:
+    """y = W x in fp64; W bf16 bits [rows, cols], x bf16 bits [cols]."""
+    lib = _load()
+    w, x = _c(w, np.uint16), _c(x, np.uint16)
+    rows, cols = w.shape
+    assert x.shape == (cols,)
+    y = np.empty(rows, dtype=np.float64)
+    lib.orc_dense_matvec.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_long, ctypes.c_long,
+                                     ctypes.c_void_p]
+    lib.orc_dense_matvec(_ptr(w), _ptr(x), rows, cols, _ptr(y))
+    return y
+
+
+def quantize_q4(w):
+    """SMOE-Q4 codes, scales and biases of bf16 weights [rows, cols] (cols % 64 == 0)."""
+    lib = _load()
+    w = _c(w, np.uint16)
+    rows, cols = w.shape
+    assert cols % 64 == 0
+    codes = np.empty((rows, cols // 2), dtype=np.uint8)
+    scale = np.empty((rows, cols // 64), dtype=np.uint16)
+    bias = np.empty((rows, cols // 64), dtype=np.uint16)
+    lib.orc_quantize_q4.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_long] + [ctypes.c_void_p] * 3
+    lib.orc_quantize_q4(_ptr(w), rows, cols, _ptr(codes), _ptr(scale), _ptr(bias))
+    return codes, scale, bias

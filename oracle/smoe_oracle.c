@@ -381,3 +381,78 @@ void orc_moe_prefill_chunk(const orc_layer *L, const uint16_t *r, int T, double 
     free(logits);
     free(xn);
 }
+
+/* ---- dense bf16 matrix-vector product ------------------------------------
+ * "Optimizations" page, "Coalesced GPU Kernels -- Expert FFN and Dense
+ * Matvec": the bf16 dense matvec twin of the expert kernels, which carries
+ * decode's QKV/O projections and the LM head.  Its plain definition:
+ *   y[r] = sum_c W[r][c] * x[c],   W bf16 [rows][cols] row-major, x bf16 [cols],
+ * every product and every partial sum in fp64 (rows are independent, so the
+ * OpenMP split over rows does not change any result). */
+void orc_dense_matvec(const uint16_t *w, const uint16_t *x, long rows, long cols, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (long c = 0; c < cols; ++c)
+            acc += orc_bf16_to_f64(w[r * cols + c]) * orc_bf16_to_f64(x[c]);
+        y[r] = acc;
+    }
+}
+
+/* ---- SMOE-Q4 quantiser ----------------------------------------------------
+ * The offline step before the path: "System Overview", "The Four-Component
+ * Architecture" and "What Happens at Each Generated Token Step" (the
+ * Sculptor turns a model's routed experts into the vault's "aggressively
+ * quantised" blocks).  The pages give no formula; this project reads it as
+ * min/max affine quantisation per group of 64 consecutive weights of a row,
+ * into the Q4 storage above, every step in binary32:
+ *   mn, mx = the least and the greatest weight of the group (bf16, exact)
+ *   scale  = bf16 nearest-even of ((mx - mn) + 0) / 15
+ *   bias   = bf16 of mn + 0  (exact; the "+ 0" turns a -0 into +0)
+ *   q      = 0 where scale is 0, else rint((w - mn) / scale) clamped to
+ *            [0, 15], rint rounding halves to even.
+ * Decoding is w' = scale * q + bias, the layout's own definition. */
+static float bf16_to_f32_orc(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void orc_quantize_q4(const uint16_t *w, long rows, long cols, uint8_t *codes, uint16_t *scale,
+                     uint16_t *bias)
+{
+    const long G = 64, ng = cols / G;
+    for (long r = 0; r < rows; ++r) {
+        for (long g = 0; g < ng; ++g) {
+            const uint16_t *p = w + r * cols + g * G;
+            float mn = bf16_to_f32_orc(p[0]), mx = mn;
+            for (long i = 1; i < G; ++i) {
+                const float v = bf16_to_f32_orc(p[i]);
+                if (v < mn) mn = v;
+                if (v > mx) mx = v;
+            }
+            const float range = (mx - mn) + 0.0f;
+            const float quot = range / 15.0f;
+            const uint16_t sb = orc_f64_to_bf16((double)quot);
+            const float s = bf16_to_f32_orc(sb);
+            scale[r * ng + g] = sb;
+            bias[r * ng + g] = orc_f64_to_bf16((double)(mn + 0.0f));
+            uint8_t *cq = codes + r * (cols / 2) + g * (G / 2);
+            for (long i = 0; i < G; ++i) {
+                int q = 0;
+                if (s != 0.0f) {
+                    const float d = bf16_to_f32_orc(p[i]) - mn;
+                    const float t = rintf(d / s);
+                    q = t < 0.0f ? 0 : (t > 15.0f ? 15 : (int)t);
+                }
+                if (i & 1)
+                    cq[i / 2] = (uint8_t)(cq[i / 2] | (q << 4));
+                else
+                    cq[i / 2] = (uint8_t)q;
+            }
+        }
+    }
+}

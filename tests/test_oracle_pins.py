@@ -323,3 +323,104 @@ def test_hand_worked_layer(oracle_mod):
                                rtol=1e-14)
     np.testing.assert_allclose(out["y"], float(g["expect_y"][0]), rtol=1e-15)
     assert np.all(out["y_bf16"] == int(g["expect_y_bf16"][0], 16))
+
+
+# ---------------------------------------------------------------- dense bf16 matvec
+
+def _bf16_bits(v):
+    return bits(torch.tensor(np.asarray(v, dtype=np.float32)).to(torch.bfloat16))
+
+
+def test_dense_matvec_one_hot_rows_pick_inputs(oracle_mod):
+    """Row r of W is one-hot at column (7 r + 3) mod cols: y[r] = x[that column]
+    exactly (a transposed operand or a shifted index fails)."""
+    rows, cols = 37, 24
+    W = np.zeros((rows, cols), dtype=np.float32)
+    pick = (7 * np.arange(rows) + 3) % cols
+    W[np.arange(rows), pick] = 1.0
+    x = np.linspace(-3.0, 5.0, cols).astype(np.float32)
+    xb = _bf16_bits(x)
+    y = oracle_mod.dense_matvec(_bf16_bits(W), xb)
+    assert np.array_equal(y, bf16_f64(xb)[pick])
+
+
+def test_dense_matvec_closed_form(oracle_mod):
+    """W[r][c] = r + 1 (every column), x[c] = c: y[r] = (r + 1) * cols (cols - 1) / 2."""
+    rows, cols = 5, 64
+    W = np.repeat(np.arange(1, rows + 1, dtype=np.float32)[:, None], cols, axis=1)
+    x = np.arange(cols, dtype=np.float32)
+    y = oracle_mod.dense_matvec(_bf16_bits(W), _bf16_bits(x))
+    assert np.array_equal(y, (np.arange(1, rows + 1) * cols * (cols - 1) / 2).astype(np.float64))
+
+
+def test_dense_matvec_matches_numpy_matmul(oracle_mod):
+    g = torch.Generator().manual_seed(21)
+    W = bits(torch.randn(33, 200, generator=g).to(torch.bfloat16))
+    x = bits(torch.randn(200, generator=g).to(torch.bfloat16))
+    ref = bf16_f64(W) @ bf16_f64(x)
+    y = oracle_mod.dense_matvec(W, x)
+    scale = np.abs(bf16_f64(W)) @ np.abs(bf16_f64(x))
+    assert np.all(np.abs(y - ref) <= 1e-13 * scale)
+
+
+# ---------------------------------------------------------------- SMOE-Q4 quantiser
+
+def _codes_of(codes_row):
+    """Unpack one row of Q4 codes: element 2j is the low nibble of byte j."""
+    c = np.asarray(codes_row, dtype=np.uint8)
+    return np.stack([c & 0x0F, c >> 4], axis=-1).reshape(-1)
+
+
+def test_quantize_ladder_is_exact(oracle_mod):
+    """A group holding 1 + 0.5 k (k = 0..15, four times) has min 1, max 8.5:
+    scale 0.5, bias 1 and codes k, all exact; a second group shifted by -4."""
+    k = np.arange(64) % 16
+    W = np.stack([np.concatenate([1.0 + 0.5 * k, -3.0 + 0.5 * k])]).astype(np.float32)
+    codes, scale, bias = oracle_mod.quantize_q4(_bf16_bits(W))
+    assert np.array_equal(bf16_f64(scale), [[0.5, 0.5]])
+    assert np.array_equal(bf16_f64(bias), [[1.0, -3.0]])
+    assert np.array_equal(_codes_of(codes[0]), np.concatenate([k, k]))
+
+
+def test_quantize_constant_group(oracle_mod):
+    """Equal weights: scale 0, every code 0, bias = the weight (a zero range
+    never divides)."""
+    W = np.full((2, 64), -1.25, dtype=np.float32)
+    W[1] = 0.0
+    codes, scale, bias = oracle_mod.quantize_q4(_bf16_bits(W))
+    assert np.all(scale == 0) and np.all(codes == 0)
+    assert np.array_equal(bf16_f64(bias)[:, 0], [-1.25, 0.0])
+    assert bias[1, 0] == 0x0000                    # +0, not -0
+
+
+def test_quantize_rounds_halves_to_even(oracle_mod):
+    """min 0, max 15 gives scale 1: 2.5 -> 2, 3.5 -> 4, 4.5 -> 4, 14.5 -> 14."""
+    W = np.zeros((1, 64), dtype=np.float32)
+    W[0, 1] = 15.0
+    W[0, 2:6] = [2.5, 3.5, 4.5, 14.5]
+    codes, scale, bias = oracle_mod.quantize_q4(_bf16_bits(W))
+    assert bf16_f64(scale)[0, 0] == 1.0 and bf16_f64(bias)[0, 0] == 0.0
+    assert list(_codes_of(codes[0])[:6]) == [0, 15, 2, 4, 4, 14]
+
+
+def test_quantize_round_trip_error_bound(oracle_mod):
+    """Random groups: every weight decodes to within half a (rounded) scale
+    step plus binary32 slack, the least weight decodes exactly, and the codes
+    are the nearest of the 16 levels wherever that level is within [0, 15]."""
+    g = torch.Generator().manual_seed(8)
+    W = torch.randn(12, 256, generator=g) * torch.exp(torch.randn(12, 1, generator=g))
+    Wb = bits(W.to(torch.bfloat16))
+    codes, scale, bias = oracle_mod.quantize_q4(Wb)
+    w = bf16_f64(Wb).reshape(12, 4, 64)
+    s = bf16_f64(scale)[:, :, None]
+    b = bf16_f64(bias)[:, :, None]
+    q = np.stack([_codes_of(codes[r]) for r in range(12)]).reshape(12, 4, 64).astype(np.float64)
+    dec = s * q + b
+    assert np.all(np.abs(dec - w) <= s * (0.5 + 2.0 ** -16))
+    assert np.array_equal(b[:, :, 0], w.min(axis=2))
+    levels = s * np.arange(16)[None, None, :] + b              # [12, 4, 16]
+    best = np.abs(w[..., None] - levels[:, :, None, :]).argmin(axis=-1)
+    gap = np.abs(w[..., None] - levels[:, :, None, :])
+    gap.sort(axis=-1)
+    clear = gap[..., 1] - gap[..., 0] > 1e-6 * s               # no near-tie
+    assert np.array_equal(q[clear], best[clear])
