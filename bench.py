@@ -39,6 +39,7 @@ import torch  # noqa: E402
 METRIC = ("MoE decode tokens/s (b=1) + expert-FFN effective HBM GB/s vs peak; prefill tok/s")
 D30, E, K, F30, L30 = 2048, 128, 8, 768, 48
 D235, F235, L235 = 4096, 1536, 94
+E30Q = (E, F30, D30)                      # a 30B layer's gate tensor, [E][F][D]
 SEED = 1337
 PER_LAYER = False   # --per-layer: decode through one smoe_moe_decode call per layer
 
@@ -349,6 +350,72 @@ def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
     return res
 
 
+def time_dense(smoe, synth, dev, hbm_peak):
+    """The dense bf16 matvec on decode's projection shapes (Qwen3-235B: K/V
+    512 x 4096, Q 8192 x 4096, O 4096 x 8192; the LM head 151,936 x 4096) and
+    the Q4 quantiser on a 30B layer's gate tensor.  Small matrices rotate over
+    enough copies that the weights of consecutive calls exceed L2."""
+    out = {}
+    shapes = {"kv_proj_512x4096": (512, 4096), "q_proj_8192x4096": (8192, 4096),
+              "o_proj_4096x8192": (4096, 8192), "lm_head_151936x4096": (151936, 4096)}
+    for name, (rows, cols) in shapes.items():
+        nbytes = rows * cols * 2
+        copies = max(1, -(-(256 << 20) // nbytes)) if nbytes < (256 << 20) else 1
+        Ws = [synth.dense_weights((rows, cols), seed=SEED + i, device=dev) for i in range(copies)]
+        x = synth.hidden(1, cols, seed=SEED, device=dev)[0]
+        y = torch.empty(rows, dtype=torch.float32, device=dev)
+        calls = max(8, copies)                 # one graph: back-to-back calls over the copies
+
+        def run():
+            for i in range(calls):
+                smoe.smoe_dense_matvec(Ws[i % copies], x, y)
+
+        g = capture(run)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, 64 // calls)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * calls)
+        del g
+        gbs = (nbytes + cols * 2 + rows * 4) / (us / 1e6) / 1e9
+        out[name] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+                     "weight_copies": copies}
+        del Ws
+        torch.cuda.empty_cache()
+    dense = {"kernel": "k_dense_matvec (bf16 weights, fp32 sums), one launch per call",
+             "timing": "CUDA graph of back-to-back calls (programmatic dependent launches), per call",
+             "shapes": out}
+    E, F, D = E30Q
+    W = synth.dense_weights((E, F, D), seed=SEED, device=dev)
+    codes = torch.empty((E, F, D // 2), dtype=torch.uint8, device=dev)
+    scale = torch.empty((E, F, D // 64), dtype=torch.bfloat16, device=dev)
+    bias = torch.empty_like(scale)
+    for _ in range(3):
+        smoe.smoe_quantize_q4(W, codes, scale, bias)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        smoe.smoe_quantize_q4(W, codes, scale, bias)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nb = W.numel() * 2 + codes.numel() + scale.numel() * 4
+    quant = {"kernel": "k_quantize_q4", "workload": f"30B layer gate tensor {E}x{F}x{D} bf16 -> SMOE-Q4",
+             "ms": round(ms, 4), "gbs": round(nb / (ms / 1e3) / 1e9, 1),
+             "frac": round(nb / (ms / 1e3) / 1e9 / hbm_peak, 4), "bytes": nb}
+    del W, codes, scale, bias
+    torch.cuda.empty_cache()
+    return dense, quant
+
+
 def cpu_baseline_oracle(stack, states, n_tokens, n_layers):
     """The oracle (as it stands) on n_tokens decode tokens through the first
     n_layers of the same stack, tokens in parallel on the host cores; the rate
@@ -398,6 +465,30 @@ def profile_case(args):
         smoe.smoe_moe_prefill_chunk(L, x64, 64, y64, ws=stack.ws)
     torch.cuda.synchronize()
     log(f"[bench] profile case done: {n} layers of {shape}")
+
+
+def profile_dense():
+    """Small case for ncu captures of the dense kernels: each matvec shape once
+    (K/V, Q, O projections, the LM head) and the quantiser on one 30B gate
+    tensor.  Prints no JSON line."""
+    dev = torch.device("cuda", 0)
+    from quantised_expert_ffn_gb300 import build
+    build.build()
+    from quantised_expert_ffn_gb300 import smoe, synth
+    for rows, cols in ((512, 4096), (8192, 4096), (4096, 8192), (151936, 4096)):
+        W = synth.dense_weights((rows, cols), seed=SEED, device=dev)
+        x = synth.hidden(1, cols, seed=SEED, device=dev)[0]
+        y = torch.empty(rows, dtype=torch.float32, device=dev)
+        smoe.smoe_dense_matvec(W, x, y)
+        torch.cuda.synchronize()
+        del W
+    E_, F_, D_ = E30Q
+    W = synth.dense_weights((E_, F_, D_), seed=SEED, device=dev)
+    codes = torch.empty((E_, F_, D_ // 2), dtype=torch.uint8, device=dev)
+    scale = torch.empty((E_, F_, D_ // 64), dtype=torch.bfloat16, device=dev)
+    smoe.smoe_quantize_q4(W, codes, scale, torch.empty_like(scale))
+    torch.cuda.synchronize()
+    log("[bench] dense profile case done")
 
 
 def our_arm(args):
@@ -475,6 +566,10 @@ def our_arm(args):
                                                        args.cpu_layers)
     del stack
     torch.cuda.empty_cache()
+
+    if rank == 0 and ws_ == 1:
+        log("[bench] dense matvec and quantiser")
+        line["dense_matvec"], line["quantize_q4"] = time_dense(smoe, synth, dev, hbm_peak)
 
     if rank == 0 and ws_ == 1 and not args.no_235b:
         log(f"[bench] building 235B stack ({L235} layers, ~128 GB)")
@@ -566,11 +661,16 @@ def main():
     ap.add_argument("--profile-layers", type=int, default=0,
                     help="run only the small ncu case with this many layers")
     ap.add_argument("--profile-shape", default="30b", choices=["30b", "235b"])
+    ap.add_argument("--profile-dense", action="store_true",
+                    help="run the dense matvec shapes and the quantiser once (for ncu), no JSON line")
     args = ap.parse_args()
     global PER_LAYER
     PER_LAYER = args.per_layer
     if args.profile_layers:
         profile_case(args)
+        return
+    if args.profile_dense:
+        profile_dense()
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -231,6 +231,40 @@ int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_de
 int smoe_moe_decode_noalloc(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
                             int32_t *idx_out_opt, float *w_out_opt, smoe_stream stream);
 
+/* Dense bf16 matrix-vector product, y[r] = sum_c w[r][c] * x[c], fp32 sums.
+ * "Optimizations" page, "Coalesced GPU Kernels -- Expert FFN and Dense
+ * Matvec": the bf16 dense matvec twin of the expert kernels, which carries
+ * decode's QKV/O projections and the LM head (shapes such as 512 x 4096 and
+ * 151,936 x 4096).  w bf16 [rows][cols] row-major and x bf16 [cols], both
+ * 16-byte aligned; y fp32 [rows], 4-byte aligned; all caller-owned device
+ * memory, read (w, x) or written (y) once.  rows >= 1; cols a multiple of 8
+ * and at most 8192 (else SMOE_ERR_UNSUPPORTED).  No workspace; nothing is
+ * allocated.  The sums run in fp32 (each lane's chunks in two partial sums,
+ * a warp tree, then the 8 warp sums in order). */
+int smoe_dense_matvec(const smoe_bf16 *w, const smoe_bf16 *x, int rows, int cols, float *y,
+                      smoe_stream stream);
+
+/* SMOE-Q4 quantiser: bf16 weights -> the Q4 layout above.  The offline step
+ * before the path ("System Overview", "The Four-Component Architecture": the
+ * Sculptor writes the routed experts as quantised vault blocks); the pages
+ * give no formula, this library fixes it as min/max affine per group of 64
+ * consecutive weights of a row:
+ *   mn, mx = least and greatest weight of the group;
+ *   scale  = bf16 (nearest, ties to even) of binary32 ((mx - mn) + 0) / 15;
+ *   bias   = mn + 0 (exact in bf16; -0 becomes +0);
+ *   q      = the integer nearest (halves to even) to d * r, with d = w - mn
+ *            rounded to binary32, r = the binary32 reciprocal of scale, the
+ *            product exact; the binary32 quotient d / scale instead where
+ *            scale is below 2^-126; 0 wherever scale is 0.  Every code is the
+ *            nearest of the 16 levels up to 2^-20 of a half step.
+ * w bf16 [rows][cols] (16-byte aligned); codes uint8 [rows][cols/2]
+ * (16-byte aligned), scale and bias bf16 [rows][cols/64]; caller-owned device
+ * memory.  cols a multiple of 64 (else SMOE_ERR_UNSUPPORTED), rows >= 1.
+ * Weights must be finite.  An expert tensor [E][rows][cols] is one call with
+ * rows = E * rows. */
+int smoe_quantize_q4(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smoe_bf16 *scale,
+                     smoe_bf16 *bias, smoe_stream stream);
+
 /* Name of the last CUDA error behind an SMOE_ERR_CUDA returned on this host
  * thread ("cudaSuccess" if none), for diagnostics. */
 const char *smoe_last_cuda_error(void);

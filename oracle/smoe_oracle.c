@@ -406,12 +406,20 @@ void orc_dense_matvec(const uint16_t *w, const uint16_t *x, long rows, long cols
  * Sculptor turns a model's routed experts into the vault's "aggressively
  * quantised" blocks).  The pages give no formula; this project reads it as
  * min/max affine quantisation per group of 64 consecutive weights of a row,
- * into the Q4 storage above, every step in binary32:
+ * into the Q4 storage above, in binary32 with one explicit exception:
  *   mn, mx = the least and the greatest weight of the group (bf16, exact)
  *   scale  = bf16 nearest-even of ((mx - mn) + 0) / 15
  *   bias   = bf16 of mn + 0  (exact; the "+ 0" turns a -0 into +0)
- *   q      = 0 where scale is 0, else rint((w - mn) / scale) clamped to
- *            [0, 15], rint rounding halves to even.
+ *   d      = w - mn, rounded to binary32
+ *   q      = 0 where scale is 0; else the integer nearest (halves to even) to
+ *            d * r, r = the binary32 reciprocal of scale (nearest), the
+ *            product taken exactly (rounded once, to the integer); where scale
+ *            is below 2^-126 (no finite binary32 reciprocal is safe), the
+ *            integer nearest to the binary32 quotient d / scale.  q is clamped
+ *            to [0, 15] (d * r <= 15.03, so the clamp never acts in practice).
+ * A quotient by multiplication with the reciprocal is how the quantiser is
+ * computed fast; rounding the exact product once keeps every code the
+ * nearest level of d / scale up to 2^-20 of a half.
  * Decoding is w' = scale * q + bias, the layout's own definition. */
 static float bf16_to_f32_orc(uint16_t h)
 {
@@ -445,8 +453,14 @@ void orc_quantize_q4(const uint16_t *w, long rows, long cols, uint8_t *codes, ui
                 int q = 0;
                 if (s != 0.0f) {
                     const float d = bf16_to_f32_orc(p[i]) - mn;
-                    const float t = rintf(d / s);
-                    q = t < 0.0f ? 0 : (t > 15.0f ? 15 : (int)t);
+                    double t;
+                    if (s >= 0x1p-126f) {
+                        const float r = 1.0f / s;
+                        t = rint((double)d * (double)r);   /* 24 x 24 bits: exact in binary64 */
+                    } else {
+                        t = rint((double)(d / s));
+                    }
+                    q = t < 0.0 ? 0 : (t > 15.0 ? 15 : (int)t);
                 }
                 if (i & 1)
                     cq[i / 2] = (uint8_t)(cq[i / 2] | (q << 4));

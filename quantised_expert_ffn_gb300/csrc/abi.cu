@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "dense.h"
 #include "kernels.h"
 
 namespace smoe {
@@ -398,6 +399,24 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
 }
 
 const char *smoe_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
+
+int smoe_dense_matvec(const smoe_bf16 *w, const smoe_bf16 *x, int rows, int cols, float *y,
+                      smoe_stream stream) {
+    if (!w || !x || !y || rows < 1 || cols < 1) return SMOE_ERR_INVALID_ARG;
+    if (cols % 8 || cols > kMaxD) return SMOE_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4)) return SMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_dense_matvec(w, x, rows, cols, y, (cudaStream_t)stream));
+}
+
+int smoe_quantize_q4(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smoe_bf16 *scale,
+                     smoe_bf16 *bias, smoe_stream stream) {
+    if (!w || !codes || !scale || !bias || rows < 1 || cols < 1) return SMOE_ERR_INVALID_ARG;
+    if (cols % kGroup) return SMOE_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scale, 2) || !aligned(bias, 2))
+        return SMOE_ERR_INVALID_ARG;
+    const long long n_groups = (long long)rows * (cols / kGroup);
+    return cuda_status(launch_quantize_q4(w, n_groups, codes, scale, bias, (cudaStream_t)stream));
+}
 
 const char *smoe_status_string(int status) {
     switch (status) {

@@ -75,6 +75,8 @@ def _load():
         "smoe_moe_decode_noalloc": (I, [LP, P, P, P, P, P]),
         "smoe_moe_decode_layers": (I, [LP, P, I, P, P, P, P, P, Z, P]),
         "smoe_last_cuda_error": (ctypes.c_char_p, []),
+        "smoe_dense_matvec": (I, [P, P, I, I, P, P]),
+        "smoe_quantize_q4": (I, [P, I, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -87,7 +89,7 @@ _lib = _load()
 EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_status",
             "smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_ffn_decode",
             "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc",
-            "smoe_last_cuda_error", "smoe_moe_decode_layers")
+            "smoe_last_cuda_error", "smoe_moe_decode_layers", "smoe_dense_matvec", "smoe_quantize_q4")
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -189,6 +191,23 @@ def smoe_moe_prefill_chunk(layer: Layer, x, T, y, idx_out=None, w_out=None, ws=N
     _check(_lib.smoe_moe_prefill_chunk(layer.ref, _p(x), int(T), _p(y), _p(idx_out), _p(w_out),
                                        _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "smoe_moe_prefill_chunk")
+
+
+def smoe_dense_matvec(w, x, y, stream=None):
+    """y = w @ x: w bf16 [rows, cols], x bf16 [cols], y fp32 [rows] (device tensors)."""
+    rows, cols = w.shape
+    _check(_lib.smoe_dense_matvec(_p(w), _p(x), int(rows), int(cols), _p(y), _stream(stream)),
+           "smoe_dense_matvec")
+
+
+def smoe_quantize_q4(w, codes, scale, bias, stream=None):
+    """SMOE-Q4 of bf16 weights w [..., cols]: codes uint8 [..., cols/2], scale and
+    bias bf16 [..., cols/64] (device tensors; leading dimensions flattened into rows)."""
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    _check(_lib.smoe_quantize_q4(_p(w), int(rows), int(cols), _p(codes), _p(scale), _p(bias),
+                                 _stream(stream)),
+           "smoe_quantize_q4")
 
 
 SMOE_DECODE_NOALLOC_MAX_BYTES = 512 * 1024

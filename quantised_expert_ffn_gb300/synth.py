@@ -103,6 +103,19 @@ def layer_weights(d_model: int, n_experts: int, ffn_dim: int, top_k: int = 8, *,
                         1e-6, norm_topk_prob)
 
 
+def dense_weights(shape, *, seed: int, device="cpu", std: float = 0.02,
+                  row_spread: float = 0.0) -> torch.Tensor:
+    """bf16 weights ~ N(0, std^2) of any shape (dense projections, LM head, or
+    the bf16 expert weights a quantiser takes); with row_spread > 0 each row's
+    std is further multiplied by exp(N(0, row_spread^2)) (rows of very
+    different magnitude)."""
+    g = _gen(seed, device)
+    w = torch.randn(shape, generator=g, device=device) * std
+    if row_spread > 0:
+        w *= torch.exp(torch.randn(tuple(shape[:-1]) + (1,), generator=g, device=device) * row_spread)
+    return w.to(torch.bfloat16)
+
+
 def hidden(T: int, d_model: int, *, seed: int, device="cpu") -> torch.Tensor:
     """T hidden states ~ N(0, 1) as bf16 [T, D]."""
     g = _gen(seed, device)

@@ -133,6 +133,29 @@ def test_decode_layers_rejects_bad_arguments_on_host(lib):
     assert call(host, dev_tab, 3) == lib.SMOE_ERR_UNSUPPORTED
 
 
+def test_dense_matvec_and_quantiser_reject_bad_arguments_on_host(lib):
+    so = lib._lib
+    P = ctypes.c_void_p
+    W, X, Y = P(1 << 20), P(1 << 21), P(1 << 22)
+    mv = lambda w=W, x=X, rows=512, cols=4096, y=Y: so.smoe_dense_matvec(w, x, rows, cols, y, None)
+    assert mv(w=None) == lib.SMOE_ERR_INVALID_ARG
+    assert mv(y=None) == lib.SMOE_ERR_INVALID_ARG
+    assert mv(rows=0) == lib.SMOE_ERR_INVALID_ARG
+    assert mv(cols=4100) == lib.SMOE_ERR_UNSUPPORTED                      # not a multiple of 8
+    assert mv(cols=16384) == lib.SMOE_ERR_UNSUPPORTED                     # beyond 8192
+    assert mv(w=P((1 << 20) + 8)) == lib.SMOE_ERR_INVALID_ARG             # w not 16-byte aligned
+    assert mv(x=P((1 << 21) + 2)) == lib.SMOE_ERR_INVALID_ARG
+    assert mv(y=P((1 << 22) + 2)) == lib.SMOE_ERR_INVALID_ARG
+    C, S, B = P(1 << 23), P(1 << 24), P(1 << 25)
+    qz = lambda w=W, rows=768, cols=2048, c=C, s=S, b=B: so.smoe_quantize_q4(w, rows, cols, c, s, b, None)
+    assert qz(c=None) == lib.SMOE_ERR_INVALID_ARG
+    assert qz(rows=0) == lib.SMOE_ERR_INVALID_ARG
+    assert qz(cols=2000) == lib.SMOE_ERR_UNSUPPORTED                      # not whole groups of 64
+    assert qz(w=P((1 << 20) + 2)) == lib.SMOE_ERR_INVALID_ARG
+    assert qz(c=P((1 << 23) + 8)) == lib.SMOE_ERR_INVALID_ARG              # codes not 16-byte aligned
+    assert qz(s=P((1 << 24) + 1)) == lib.SMOE_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in range(-6, 1):
         assert lib.smoe_status_string(code).startswith("SMOE_")
