@@ -9,7 +9,8 @@
 //   * CTA = 8 warps; warp w owns the w-th eighth of the 16-byte chunks of
 //     every row, lane l the chunks c0 + l + 32 j of that eighth -- a warp's
 //     loads of one row are 512 consecutive bytes, and the lane's x values stay
-//     in registers for the CTA's whole life (cols <= 8192);
+//     in registers for the CTA's whole life (in shared memory for rows of
+//     more than 4096, where registers hold the loads instead; cols <= 8192);
 //   * four CTAs per SM; CTA b owns the contiguous rows [R b / G, R (b+1) / G)
 //     (balanced to one row) and takes RB of them at a time (RB * CPL loads in
 //     flight per lane); small row counts use RB = 1 and one row per CTA so
@@ -49,11 +50,14 @@ __device__ __forceinline__ float2 bf16x2_f32(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
 
-template <int RB, int CPL>
+// XS: x stays in shared memory (bf16) instead of registers, for CPL = 4,
+// where registers would not hold both x and every load of a step.
+template <int RB, int CPL, bool XS>
 __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm)
     k_dense_matvec(const uint16_t *__restrict__ w, const uint16_t *__restrict__ x, int rows, int cols,
                    float *__restrict__ y) {
     __shared__ float part[2][RB][kMvWarps];
+    __shared__ uint4 xsm[XS ? 1024 : 1];                      // x as bf16, cols <= 8192
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int NC = cols >> 3;                                 // 16-byte chunks per row
     const int c0 = NC * warp / kMvWarps, c1 = NC * (warp + 1) / kMvWarps;
@@ -61,16 +65,21 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm)
     // previous kernel in the stream has completed
     pdl_wait();
     pdl_launch_dependents();
-    float2 xr[CPL][4];
+    float2 xr[XS ? 1 : CPL][4];
+    if (XS) {
+        for (int c = threadIdx.x; c < NC; c += kMvThreads) xsm[c] = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+        __syncthreads();
+    } else {
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        const int c = c0 + lane + 32 * j;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (c < c1) v = __ldg(reinterpret_cast<const uint4 *>(x) + c);
-        xr[j][0] = bf16x2_f32(v.x);
-        xr[j][1] = bf16x2_f32(v.y);
-        xr[j][2] = bf16x2_f32(v.z);
-        xr[j][3] = bf16x2_f32(v.w);
+        for (int j = 0; j < (XS ? 1 : CPL); ++j) {
+            const int c = c0 + lane + 32 * j;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (c < c1) v = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+            xr[j][0] = bf16x2_f32(v.x);
+            xr[j][1] = bf16x2_f32(v.y);
+            xr[j][2] = bf16x2_f32(v.z);
+            xr[j][3] = bf16x2_f32(v.w);
+        }
     }
     // CTA b owns rows [rows*b/G, rows*(b+1)/G), taken RB at a time
     const int r_beg = (int)((long long)rows * blockIdx.x / gridDim.x);
@@ -93,10 +102,22 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm)
             float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
-                a2 = ffma2(bf16x2_f32(wv[r][j].x), xr[j][0], a2);
-                a2 = ffma2(bf16x2_f32(wv[r][j].y), xr[j][1], a2);
-                a2 = ffma2(bf16x2_f32(wv[r][j].z), xr[j][2], a2);
-                a2 = ffma2(bf16x2_f32(wv[r][j].w), xr[j][3], a2);
+                float2 xj[4];
+                if (XS) {
+                    const int c = c0 + lane + 32 * j;
+                    const uint4 v = c < c1 ? xsm[c] : make_uint4(0, 0, 0, 0);
+                    xj[0] = bf16x2_f32(v.x);
+                    xj[1] = bf16x2_f32(v.y);
+                    xj[2] = bf16x2_f32(v.z);
+                    xj[3] = bf16x2_f32(v.w);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) xj[k] = xr[XS ? 0 : j][k];
+                }
+                a2 = ffma2(bf16x2_f32(wv[r][j].x), xj[0], a2);
+                a2 = ffma2(bf16x2_f32(wv[r][j].y), xj[1], a2);
+                a2 = ffma2(bf16x2_f32(wv[r][j].z), xj[2], a2);
+                a2 = ffma2(bf16x2_f32(wv[r][j].w), xj[3], a2);
             }
             acc[r] = warp_sum(a2.x + a2.y);
         }
@@ -114,11 +135,12 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm)
     }
 }
 
-template <int RB, int CPL>
+template <int RB, int CPL, bool XS = false>
 cudaError_t launch_mv(const uint16_t *w, const uint16_t *x, int rows, int cols, float *y, int grid_cap,
                       cudaStream_t s) {
     const int grid = rows < grid_cap ? rows : grid_cap;
-    return launch_kernel(k_dense_matvec<RB, CPL>, dim3(grid), dim3(kMvThreads), 0, s, true, w, x, rows, cols, y);
+    return launch_kernel(k_dense_matvec<RB, CPL, XS>, dim3(grid), dim3(kMvThreads), 0, s, true, w, x, rows, cols,
+                         y);
 }
 
 template <int RB>
@@ -127,7 +149,7 @@ cudaError_t launch_mv_rb(const uint16_t *w, const uint16_t *x, int rows, int col
     const int per_warp = ((cols >> 3) + kMvWarps - 1) / kMvWarps;   // chunks of one warp's eighth
     if (per_warp <= 32) return launch_mv<RB, 1>(w, x, rows, cols, y, grid_cap, s);
     if (per_warp <= 64) return launch_mv<RB, 2>(w, x, rows, cols, y, grid_cap, s);
-    return launch_mv<(RB > 2 ? 2 : RB), 4>(w, x, rows, cols, y, grid_cap, s);
+    return launch_mv<(RB > 2 ? 2 : RB), 4, true>(w, x, rows, cols, y, grid_cap, s);
 }
 
 // ---------------------------------------------------------------- quantiser
