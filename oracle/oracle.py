@@ -64,6 +64,7 @@ class _Layer(ctypes.Structure):
         ("down_q", ctypes.c_void_p),
         ("down_s", ctypes.c_void_p),
         ("down_b", ctypes.c_void_p),
+        ("code_bits", ctypes.c_int),
     ]
 
 
@@ -81,7 +82,8 @@ class OracleLayer:
 
     Shapes: router_w [E, D]; gate_q/up_q [E, F, D/2]; gate_s/gate_b/up_s/up_b
     [E, F, D/64]; down_q [E, D, F/2]; down_s/down_b [E, D, F/64]; rms_gain [D]
-    or None (no RMSNorm).
+    or None (no RMSNorm).  With code_bits = 2 (SMOE-Q2) the code arrays are
+    [E, F, D/4] and [E, D, F/4].
     """
     d_model: int
     n_experts: int
@@ -101,6 +103,7 @@ class OracleLayer:
     rms_eps: float = 1e-6
     norm_topk_prob: bool = True
     group_size: int = 64
+    code_bits: int = 4
 
     def __post_init__(self):
         u16, u8 = np.uint16, np.uint8
@@ -111,15 +114,17 @@ class OracleLayer:
         if self.rms_gain is not None:
             self.rms_gain = _c(self.rms_gain, u16)
         D, E, F, G = self.d_model, self.n_experts, self.ffn_dim, self.group_size
+        assert self.code_bits in (2, 4)
+        per_byte = 8 // self.code_bits
         assert self.router_w.shape == (E, D)
-        assert self.gate_q.shape == (E, F, D // 2) and self.up_q.shape == (E, F, D // 2)
+        assert self.gate_q.shape == (E, F, D // per_byte) and self.up_q.shape == (E, F, D // per_byte)
         assert self.gate_s.shape == (E, F, D // G) and self.up_b.shape == (E, F, D // G)
-        assert self.down_q.shape == (E, D, F // 2) and self.down_s.shape == (E, D, F // G)
+        assert self.down_q.shape == (E, D, F // per_byte) and self.down_s.shape == (E, D, F // G)
         self._s = _Layer(D, E, self.top_k, F, G, int(self.norm_topk_prob), float(self.rms_eps),
                          _ptr(self.rms_gain), _ptr(self.router_w),
                          _ptr(self.gate_q), _ptr(self.gate_s), _ptr(self.gate_b),
                          _ptr(self.up_q), _ptr(self.up_s), _ptr(self.up_b),
-                         _ptr(self.down_q), _ptr(self.down_s), _ptr(self.down_b))
+                         _ptr(self.down_q), _ptr(self.down_s), _ptr(self.down_b), int(self.code_bits))
 
     @property
     def ref(self):
@@ -151,6 +156,14 @@ def q4_weight(q, s, b, row, cols, col, group=64) -> float:
     lib.orc_q4_weight.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_long] * 4
     q, s, b = _c(q, np.uint8), _c(s, np.uint16), _c(b, np.uint16)
     return lib.orc_q4_weight(_ptr(q), _ptr(s), _ptr(b), row, cols, group, col)
+
+
+def q2_weight(q, s, b, row, cols, col, group=64) -> float:
+    lib = _load()
+    lib.orc_q2_weight.restype = ctypes.c_double
+    lib.orc_q2_weight.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_long] * 4
+    q, s, b = _c(q, np.uint8), _c(s, np.uint16), _c(b, np.uint16)
+    return lib.orc_q2_weight(_ptr(q), _ptr(s), _ptr(b), row, cols, group, col)
 
 
 def rmsnorm(L: OracleLayer, r) -> np.ndarray:
@@ -297,4 +310,18 @@ def quantize_q4(w):
     bias = np.empty((rows, cols // 64), dtype=np.uint16)
     lib.orc_quantize_q4.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_long] + [ctypes.c_void_p] * 3
     lib.orc_quantize_q4(_ptr(w), rows, cols, _ptr(codes), _ptr(scale), _ptr(bias))
+    return codes, scale, bias
+
+
+def quantize_q2(w):
+    """SMOE-Q2 codes ([rows, cols/4]), scales and biases of bf16 weights [rows, cols]."""
+    lib = _load()
+    w = _c(w, np.uint16)
+    rows, cols = w.shape
+    assert cols % 64 == 0
+    codes = np.empty((rows, cols // 4), dtype=np.uint8)
+    scale = np.empty((rows, cols // 64), dtype=np.uint16)
+    bias = np.empty((rows, cols // 64), dtype=np.uint16)
+    lib.orc_quantize_q2.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_long] + [ctypes.c_void_p] * 3
+    lib.orc_quantize_q2(_ptr(w), rows, cols, _ptr(codes), _ptr(scale), _ptr(bias))
     return codes, scale, bias

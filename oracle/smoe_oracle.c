@@ -42,6 +42,11 @@
  * Q4 storage (fixed by this project, since the pages leave it open):
  *   codes: row-major [rows][cols/2] bytes; element 2j is the low nibble of
  *          byte j, element 2j+1 the high nibble;
+ *   (SMOE-Q2, the pages' 2-bit vault -- "Optimizations", "Q2 Vaults -- the
+ *   Next 2x, Twice Over"; "System Overview", the "SMOE-Q2/Q4 fused dequant"
+ *   kernel: the same groups, scales and biases with 2-bit codes,
+ *   [rows][cols/4] bytes, element 4j+k in bits 2k..2k+1 of byte j; a layer
+ *   says which with code_bits, 4 or 2;)
  *   scale, bias: bf16 [rows][cols/64];
  *   per layer the experts are contiguous: gate and up [E][F][D], down [E][D][F]
  *   (rows x input columns); router bf16 [E][D].
@@ -73,6 +78,7 @@ typedef struct orc_layer {
     const uint8_t *down_q;    /* [E][D][F/2] */
     const uint16_t *down_s;   /* [E][D][F/G] */
     const uint16_t *down_b;
+    int code_bits;            /* 4 (SMOE-Q4) or 2 (SMOE-Q2); 0 reads as 4 */
 } orc_layer;
 
 /* ---- bf16 <-> double --------------------------------------------------- */
@@ -129,6 +135,29 @@ double orc_q4_weight(const uint8_t *q, const uint16_t *s, const uint16_t *b,
                      long row, long cols, long group, long col)
 {
     return q4_weight(q, s, b, row, cols, group, col);
+}
+
+/* Weight (row, col) of a Q2 matrix: code = bits 2k..2k+1 of byte col/4, k = col % 4. */
+static double q2_weight(const uint8_t *q, const uint16_t *s, const uint16_t *b,
+                        long row, long cols, long group, long col)
+{
+    uint8_t byte = q[row * (cols / 4) + col / 4];
+    int code = (byte >> (2 * (col & 3))) & 0x03;
+    long gi = row * (cols / group) + col / group;
+    return orc_bf16_to_f64(s[gi]) * (double)code + orc_bf16_to_f64(b[gi]);
+}
+
+double orc_q2_weight(const uint8_t *q, const uint16_t *s, const uint16_t *b,
+                     long row, long cols, long group, long col)
+{
+    return q2_weight(q, s, b, row, cols, group, col);
+}
+
+static double code_weight(int bits, const uint8_t *q, const uint16_t *s, const uint16_t *b,
+                          long row, long cols, long group, long col)
+{
+    return bits == 2 ? q2_weight(q, s, b, row, cols, group, col)
+                     : q4_weight(q, s, b, row, cols, group, col);
 }
 
 /* ---- step 0: RMSNorm ----------------------------------------------------- */
@@ -221,6 +250,7 @@ void orc_mix_weights(const double *logits, int E, const int32_t *idx, int k,
 void orc_expert_ffn(const orc_layer *L, int e, const uint16_t *xn, double *o, double *h_out)
 {
     long D = L->d_model, F = L->ffn_dim, G = L->group_size;
+    const int bits = L->code_bits == 2 ? 2 : 4;
     double *x = (double *)malloc(sizeof(double) * (size_t)D);
     double *h = (double *)malloc(sizeof(double) * (size_t)F);
     for (long d = 0; d < D; ++d)
@@ -229,8 +259,8 @@ void orc_expert_ffn(const orc_layer *L, int e, const uint16_t *xn, double *o, do
         long row = (long)e * F + j;
         double g = 0.0, u = 0.0;
         for (long d = 0; d < D; ++d) {
-            g += q4_weight(L->gate_q, L->gate_s, L->gate_b, row, D, G, d) * x[d];
-            u += q4_weight(L->up_q, L->up_s, L->up_b, row, D, G, d) * x[d];
+            g += code_weight(bits, L->gate_q, L->gate_s, L->gate_b, row, D, G, d) * x[d];
+            u += code_weight(bits, L->up_q, L->up_s, L->up_b, row, D, G, d) * x[d];
         }
         h[j] = g / (1.0 + exp(-g)) * u; /* SiLU(g) * u */
     }
@@ -238,7 +268,7 @@ void orc_expert_ffn(const orc_layer *L, int e, const uint16_t *xn, double *o, do
         long row = (long)e * D + d;
         double acc = 0.0;
         for (long f = 0; f < F; ++f)
-            acc += q4_weight(L->down_q, L->down_s, L->down_b, row, F, G, f) * h[f];
+            acc += code_weight(bits, L->down_q, L->down_s, L->down_b, row, F, G, f) * h[f];
         o[d] = acc;
     }
     if (h_out)
@@ -429,10 +459,15 @@ static float bf16_to_f32_orc(uint16_t h)
     return f;
 }
 
-void orc_quantize_q4(const uint16_t *w, long rows, long cols, uint8_t *codes, uint16_t *scale,
-                     uint16_t *bias)
+/* The same reading for SMOE-Q2 (bits = 2): levels = 2^bits - 1 = 3 replaces 15
+ * (scale = bf16 of ((mx - mn) + 0) / 3, codes clamped to [0, 3]), codes stored
+ * as in the Q2 layout above. */
+static void quantize_codes(const uint16_t *w, long rows, long cols, int bits, uint8_t *codes,
+                           uint16_t *scale, uint16_t *bias)
 {
     const long G = 64, ng = cols / G;
+    const int levels = (1 << bits) - 1, per_byte = 8 / bits;
+    const float flev = (float)levels;
     for (long r = 0; r < rows; ++r) {
         for (long g = 0; g < ng; ++g) {
             const uint16_t *p = w + r * cols + g * G;
@@ -443,12 +478,13 @@ void orc_quantize_q4(const uint16_t *w, long rows, long cols, uint8_t *codes, ui
                 if (v > mx) mx = v;
             }
             const float range = (mx - mn) + 0.0f;
-            const float quot = range / 15.0f;
+            const float quot = range / flev;
             const uint16_t sb = orc_f64_to_bf16((double)quot);
             const float s = bf16_to_f32_orc(sb);
             scale[r * ng + g] = sb;
             bias[r * ng + g] = orc_f64_to_bf16((double)(mn + 0.0f));
-            uint8_t *cq = codes + r * (cols / 2) + g * (G / 2);
+            uint8_t *cq = codes + r * (cols / per_byte) + g * (G / per_byte);
+            memset(cq, 0, (size_t)(G / per_byte));
             for (long i = 0; i < G; ++i) {
                 int q = 0;
                 if (s != 0.0f) {
@@ -460,13 +496,22 @@ void orc_quantize_q4(const uint16_t *w, long rows, long cols, uint8_t *codes, ui
                     } else {
                         t = rint((double)(d / s));
                     }
-                    q = t < 0.0 ? 0 : (t > 15.0 ? 15 : (int)t);
+                    q = t < 0.0 ? 0 : (t > (double)levels ? levels : (int)t);
                 }
-                if (i & 1)
-                    cq[i / 2] = (uint8_t)(cq[i / 2] | (q << 4));
-                else
-                    cq[i / 2] = (uint8_t)q;
+                cq[i / per_byte] = (uint8_t)(cq[i / per_byte] | (q << (bits * (i % per_byte))));
             }
         }
     }
+}
+
+void orc_quantize_q4(const uint16_t *w, long rows, long cols, uint8_t *codes, uint16_t *scale,
+                     uint16_t *bias)
+{
+    quantize_codes(w, rows, cols, 4, codes, scale, bias);
+}
+
+void orc_quantize_q2(const uint16_t *w, long rows, long cols, uint8_t *codes, uint16_t *scale,
+                     uint16_t *bias)
+{
+    quantize_codes(w, rows, cols, 2, codes, scale, bias);
 }

@@ -11,11 +11,15 @@ weights; no checkpoint is used):
   * SMOE-Q4 codes uniform in 0..15 (so every byte, two codes, is uniform in
     0..255), scale = bf16(|N(0, 0.02)| / 8), bias = -8 * scale (exact in bf16),
     one scale and one bias per group of 64 along the input dimension;
-  * RMSNorm gain of ones when a norm is requested.
+  * RMSNorm gain of ones when a norm is requested;
+  * SMOE-Q2 (code_bits=2): codes uniform in 0..3 (every byte, four codes,
+    uniform in 0..255), scale = bf16(|N(0, 0.02)| / 2), bias = -2 * scale
+    (exact), so a weight has about the spread of the Q4 draw.
 
 Storage layout (fixed by this project): codes row-major [rows, cols/2] with
 element 2j in the low nibble of byte j and 2j+1 in the high nibble; scales and
-biases [rows, cols/64]; gate and up [E, F, D]; down [E, D, F].
+biases [rows, cols/64]; gate and up [E, F, D]; down [E, D, F].  SMOE-Q2 codes
+are [rows, cols/4], element 4j+k in bits 2k..2k+1 of byte j.
 """
 from __future__ import annotations
 
@@ -46,6 +50,7 @@ class LayerWeights:
     rms_gain: Optional[torch.Tensor] = None   # bf16 [D] or None
     rms_eps: float = 1e-6
     norm_topk_prob: bool = True
+    code_bits: int = 4                         # 4: SMOE-Q4, 2: SMOE-Q2
 
     def tensors(self) -> List[torch.Tensor]:
         out = [self.router_w, self.gate_q, self.gate_s, self.gate_b, self.up_q, self.up_s,
@@ -73,34 +78,36 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
-def _scales(shape, g, device):
-    s = (torch.randn(shape, generator=g, device=device, dtype=torch.float32).abs_() * (0.02 / 8)
+def _scales(shape, g, device, code_bits=4):
+    div, mid = (8.0, -8.0) if code_bits == 4 else (2.0, -2.0)
+    s = (torch.randn(shape, generator=g, device=device, dtype=torch.float32).abs_() * (0.02 / div)
          ).to(torch.bfloat16)
-    return s, (s.float() * -8.0).to(torch.bfloat16)
+    return s, (s.float() * mid).to(torch.bfloat16)
 
 
 def layer_weights(d_model: int, n_experts: int, ffn_dim: int, top_k: int = 8, *, seed: int,
-                  device="cpu", rms_norm: bool = False, norm_topk_prob: bool = True
-                  ) -> LayerWeights:
+                  device="cpu", rms_norm: bool = False, norm_topk_prob: bool = True,
+                  code_bits: int = 4) -> LayerWeights:
     """One layer of seeded weights (see the module docstring)."""
     D, E, F = d_model, n_experts, ffn_dim
-    assert D % GROUP == 0 and F % GROUP == 0
+    assert D % GROUP == 0 and F % GROUP == 0 and code_bits in (2, 4)
+    per_byte = 8 // code_bits
     g = _gen(seed, device)
     router = (torch.randn((E, D), generator=g, device=device) * 0.02).to(torch.bfloat16)
 
     def codes(rows, cols):
-        return torch.randint(0, 256, (E, rows, cols // 2), generator=g, device=device,
+        return torch.randint(0, 256, (E, rows, cols // per_byte), generator=g, device=device,
                              dtype=torch.uint8)
 
     gq = codes(F, D)
-    gs, gb = _scales((E, F, D // GROUP), g, device)
+    gs, gb = _scales((E, F, D // GROUP), g, device, code_bits)
     uq = codes(F, D)
-    us, ub = _scales((E, F, D // GROUP), g, device)
+    us, ub = _scales((E, F, D // GROUP), g, device, code_bits)
     dq = codes(D, F)
-    ds, db = _scales((E, D, F // GROUP), g, device)
+    ds, db = _scales((E, D, F // GROUP), g, device, code_bits)
     gain = torch.ones(D, dtype=torch.bfloat16, device=device) if rms_norm else None
     return LayerWeights(D, E, top_k, F, router, gq, gs, gb, uq, us, ub, dq, ds, db, gain,
-                        1e-6, norm_topk_prob)
+                        1e-6, norm_topk_prob, code_bits)
 
 
 def dense_weights(shape, *, seed: int, device="cpu", std: float = 0.02,

@@ -424,3 +424,92 @@ def test_quantize_round_trip_error_bound(oracle_mod):
     gap.sort(axis=-1)
     clear = gap[..., 1] - gap[..., 0] > 1e-6 * s               # no near-tie
     assert np.array_equal(q[clear], best[clear])
+
+
+# ---------------------------------------------------------------- SMOE-Q2 layout
+
+def _set_code2(q, row, col, code):
+    sh = 2 * (col % 4)
+    q[row, col // 4] = (int(q[row, col // 4]) & ~(3 << sh) & 0xFF) | (code << sh)
+
+
+def test_q2_single_code_pins_layout(oracle_mod):
+    """SMOE-Q2: every code 2 with bias -2 s gives w = 0; one code moved to 3 in
+    gate (row 6, col 71) and to 0 in down (row 33, col 6): g is zero except
+    g[6] = s_g x[71], o zero except o[33] = -2 s_d h[6].  Distinct scales per
+    group and the 2-bit position (col % 4 = 3, then 2) make a wrong group,
+    shift or transposition show."""
+    D, F = 128, 64
+    W = synth.layer_weights(D, 1, F, 1, seed=0, code_bits=2)
+    for n in ("gate_q", "up_q", "down_q"):
+        getattr(W, n).fill_(0xAA)                      # every code 2
+    gs = (torch.arange(F * D // 64, dtype=torch.float32).reshape(1, F, D // 64) + 1) / 256
+    W.gate_s = gs.to(torch.bfloat16)
+    W.gate_b = (W.gate_s.float() * -2).to(torch.bfloat16)
+    W.up_s = torch.zeros_like(W.up_s)
+    W.up_b = torch.full_like(W.up_b, 1 / 64)
+    ds = (torch.arange(D * F // 64, dtype=torch.float32).reshape(1, D, F // 64) + 3) / 512
+    W.down_s = ds.to(torch.bfloat16)
+    W.down_b = (W.down_s.float() * -2).to(torch.bfloat16)
+    j0, d0, d1 = 6, 71, 33
+    _set_code2(W.gate_q[0], j0, d0, 3)
+    _set_code2(W.down_q[0], d1, j0, 0)
+    L = oracle_layer(W)
+    assert L.code_bits == 2
+    x = bits(synth.hidden(1, D, seed=11))[0]
+    xf = bf16_f64(x)
+    o, h = oracle_mod.expert_ffn(L, 0, x)
+    g = float(W.gate_s[0, j0, d0 // 64]) * xf[d0]
+    hj = g * scipy.special.expit(g) * (xf.sum() / 64)
+    assert np.count_nonzero(h) == 1 and h[j0] == pytest.approx(hj, rel=1e-13)
+    s_d = float(W.down_s[0, d1, j0 // 64])
+    assert np.count_nonzero(o) == 1 and o[d1] == pytest.approx(-2 * s_d * hj, rel=1e-13)
+
+
+def _numpy_dequant_q2(q, s, b):
+    """Independent unpack of the documented Q2 layout with numpy."""
+    codes = np.stack([(q >> (2 * k)) & 3 for k in range(4)], axis=-1).reshape(q.shape[0], -1)
+    return codes.astype(np.float64) * np.repeat(bf16_f64(s), 64, axis=1) + np.repeat(bf16_f64(b), 64, axis=1)
+
+
+def test_q2_expert_ffn_matches_numpy_matmul(oracle_mod):
+    D, F, E = 128, 192, 2
+    W = synth.layer_weights(D, E, F, 2, seed=22, code_bits=2)
+    W.up_b = (torch.randn(W.up_b.shape) * 0.01).to(torch.bfloat16)
+    W.down_b = (torch.randn(W.down_b.shape) * 0.01).to(torch.bfloat16)
+    L = oracle_layer(W)
+    x = bits(synth.hidden(1, D, seed=5))[0]
+    xf = bf16_f64(x)
+    for e in range(E):
+        Wg = _numpy_dequant_q2(L.gate_q[e], L.gate_s[e], L.gate_b[e])
+        Wu = _numpy_dequant_q2(L.up_q[e], L.up_s[e], L.up_b[e])
+        Wd = _numpy_dequant_q2(L.down_q[e], L.down_s[e], L.down_b[e])
+        g, u = Wg @ xf, Wu @ xf
+        h_ref = g * scipy.special.expit(g) * u
+        o, h = oracle_mod.expert_ffn(L, e, x)
+        np.testing.assert_allclose(h, h_ref, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(o, Wd @ h_ref, rtol=1e-11, atol=1e-14)
+
+
+def test_q2_weight_reads_the_documented_bits(oracle_mod):
+    """Byte 0b11_10_01_00 holds codes 0, 1, 2, 3 for columns 0..3."""
+    q = np.array([[0b11100100] + [0] * 15], dtype=np.uint8)
+    s = _bf16_bits([[1.0]])
+    b = _bf16_bits([[0.5]])
+    assert [oracle_mod.q2_weight(q, s, b, 0, 64, c) for c in range(4)] == [0.5, 1.5, 2.5, 3.5]
+
+
+def test_quantize_q2_ladder_and_ties(oracle_mod):
+    """Q2: a group of 1 + 0.25 k (k = 0..3) has scale 0.25, bias 1, codes k; a
+    group with min 0, max 3 and halves 0.5, 1.5, 2.5 rounds them to 0, 2, 2."""
+    k = np.arange(64) % 4
+    W = np.zeros((2, 64), dtype=np.float32)
+    W[0] = 1.0 + 0.25 * k
+    W[1, 1] = 3.0
+    W[1, 2:5] = [0.5, 1.5, 2.5]
+    codes, scale, bias = oracle_mod.quantize_q2(_bf16_bits(W))
+    assert np.array_equal(bf16_f64(scale)[:, 0], [0.25, 1.0])
+    assert np.array_equal(bf16_f64(bias)[:, 0], [1.0, 0.0])
+    unpack = lambda row: np.stack([(codes[row] >> (2 * j)) & 3 for j in range(4)], -1).reshape(-1)
+    assert np.array_equal(unpack(0), k)
+    assert list(unpack(1)[:5]) == [0, 3, 0, 2, 2]

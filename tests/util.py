@@ -31,7 +31,7 @@ def oracle_layer(W) -> OracleLayer:
         gate_b=host(W.gate_b), up_q=host(W.up_q), up_s=host(W.up_s), up_b=host(W.up_b),
         down_q=host(W.down_q), down_s=host(W.down_s), down_b=host(W.down_b),
         rms_gain=None if W.rms_gain is None else host(W.rms_gain), rms_eps=W.rms_eps,
-        norm_topk_prob=W.norm_topk_prob)
+        norm_topk_prob=W.norm_topk_prob, code_bits=getattr(W, "code_bits", 4))
 
 
 def bf16_f64(a: np.ndarray) -> np.ndarray:
