@@ -63,9 +63,9 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def expert_bytes(D, F):
+def expert_bytes(D, F, code_bits=4):
     # codes + bf16 scale + bf16 bias for gate, up (F x D) and down (D x F)
-    per_matrix = D * F // 2 + 2 * 2 * (D * F // 64)
+    per_matrix = D * F * code_bits // 8 + 2 * 2 * (D * F // 64)
     return 3 * per_matrix
 
 
@@ -173,9 +173,10 @@ def dist_env():
 class DecodeStack:
     """A stack of decode layers driven through the C ABI (one shared workspace)."""
 
-    def __init__(self, smoe, synth, n_layers, D, F, seed, dev):
+    def __init__(self, smoe, synth, n_layers, D, F, seed, dev, code_bits=4):
         self.smoe = smoe
-        self.W = [synth.layer_weights(D, E, F, K, seed=seed * 1000 + i, device=dev, rms_norm=True)
+        self.W = [synth.layer_weights(D, E, F, K, seed=seed * 1000 + i, device=dev, rms_norm=True,
+                                      code_bits=code_bits)
                   for i in range(n_layers)]
         self.L = [smoe.Layer(w) for w in self.W]
         self.table = smoe.LayerTable(self.L, dev)
@@ -568,6 +569,18 @@ def our_arm(args):
     torch.cuda.empty_cache()
 
     if rank == 0 and ws_ == 1:
+        log(f"[bench] building 30B SMOE-Q2 stack ({L30} layers)")
+        q2 = DecodeStack(smoe, synth, L30, D30, F30, SEED + 2, dev, code_bits=2)
+        msq2, _ = time_decode(q2, states, 256, 16, 16)
+        bq2 = L30 * (K * expert_bytes(D30, F30, 2) + E * D30 * 2)
+        line["decode_q2"] = {"workload": "30B-shaped 48-layer decode stack with SMOE-Q2 experts (2-bit "
+                                         "codes, same groups), batch 1, 256 tokens",
+                             "tok_s": round(1e3 / msq2, 2), "ms_per_token": round(msq2, 4),
+                             "us_per_layer": round(msq2 * 1e3 / L30, 2),
+                             "effective_gbs": round(bq2 / (msq2 / 1e3) / 1e9, 1),
+                             "bytes_per_token": bq2}
+        del q2
+        torch.cuda.empty_cache()
         log("[bench] dense matvec and quantiser")
         line["dense_matvec"], line["quantize_q4"] = time_dense(smoe, synth, dev, hbm_peak)
 

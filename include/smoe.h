@@ -42,6 +42,16 @@
  * (codes [E][F][D/2], scale/bias [E][F][D/64]); down is [E][D][F]
  * (codes [E][D][F/2], scale/bias [E][D][F/64]); the router is bf16 [E][D].
  *
+ * SMOE-Q2 weights ("Optimizations", "Q2 Vaults -- the Next 2x, Twice Over":
+ * the 2-bit vault that halves every blob; "System Overview", the "SMOE-Q2/Q4
+ * fused dequant + FFN" kernel).  A layer with code_bits = 2 keeps the groups,
+ * scales and biases above with 2-bit codes q in 0..3: codes uint8
+ * [rows][cols/4], element 4j+k in bits 2k..2k+1 of byte j.  Decode
+ * (smoe_moe_decode, smoe_moe_ffn_decode, smoe_moe_decode_layers,
+ * smoe_moe_decode_noalloc) takes Q2 layers whose shape fits the one-kernel
+ * decode plan (d_model a multiple of 512 up to 4096, ffn_dim a multiple of
+ * 128); other Q2 shapes and Q2 prefill return SMOE_ERR_UNSUPPORTED.
+ *
  * Workspace.  Calls that need scratch take `ws`/`ws_bytes`: device memory of
  * at least smoe_workspace_bytes() bytes, 256-byte aligned, that the caller
  * zero-fills once before its first use (smoe_workspace_init() does it on the
@@ -107,6 +117,7 @@ typedef struct smoe_layer {
     const uint8_t *down_q;       /* [E][D][F/2] */
     const smoe_bf16 *down_s;     /* [E][D][F/64] */
     const smoe_bf16 *down_b;     /* [E][D][F/64] */
+    int code_bits;               /* 4 (SMOE-Q4; 0 reads as 4) or 2 (SMOE-Q2, see below) */
 } smoe_layer;
 
 /* Bytes of workspace that the calls below need for this layer shape and up
@@ -263,6 +274,13 @@ int smoe_dense_matvec(const smoe_bf16 *w, const smoe_bf16 *x, int rows, int cols
  * Weights must be finite.  An expert tensor [E][rows][cols] is one call with
  * rows = E * rows. */
 int smoe_quantize_q4(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smoe_bf16 *scale,
+                     smoe_bf16 *bias, smoe_stream stream);
+
+/* SMOE-Q2 quantiser: the same reading with 2-bit codes, 3 levels instead of
+ * 15 -- scale = bf16 of binary32 ((mx - mn) + 0) / 3, codes clamped to
+ * [0, 3] -- into the Q2 layout above (codes uint8 [rows][cols/4], 16-byte
+ * aligned).  Arguments and errors as smoe_quantize_q4. */
+int smoe_quantize_q2(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smoe_bf16 *scale,
                      smoe_bf16 *bias, smoe_stream stream);
 
 /* Name of the last CUDA error behind an SMOE_ERR_CUDA returned on this host

@@ -63,6 +63,7 @@ int check_layer(const smoe_layer *L) {
         !L->up_b || !L->down_q || !L->down_s || !L->down_b)
         return SMOE_ERR_INVALID_ARG;
     if (L->group_size != kGroup) return SMOE_ERR_UNSUPPORTED;
+    if (L->code_bits != 0 && L->code_bits != 4 && L->code_bits != 2) return SMOE_ERR_UNSUPPORTED;
     const int D = L->d_model, E = L->n_experts, K = L->top_k, F = L->ffn_dim;
     if (D <= 0 || F <= 0 || E <= 0 || K <= 0) return SMOE_ERR_INVALID_ARG;
     if (D % kGroup || F % kGroup) return SMOE_ERR_UNSUPPORTED;
@@ -78,6 +79,8 @@ int check_layer(const smoe_layer *L) {
     if (L->rms_gain && !(L->rms_eps >= 0.f)) return SMOE_ERR_INVALID_ARG;
     return SMOE_OK;
 }
+
+bool is_q2(const smoe_layer &L) { return L.code_bits == 2; }
 
 int check_ws(const smoe_layer *L, int T, void *ws, size_t ws_bytes) {
     if (!ws || !aligned(ws, kAlign)) return SMOE_ERR_WORKSPACE;
@@ -222,8 +225,10 @@ static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int
     f.w_in = w_in;
     f.expert_out = expert_out;
     f.n_layers = 1;
+    f.q2 = is_q2(L) ? 1 : 0;
     if (decode_path() == 1 && fused_plan(f, device_sm_count()))
         return cuda_status(launch_decode_layer(f, s, idx_in == nullptr));
+    if (f.q2) return SMOE_ERR_UNSUPPORTED;                    // Q2 runs on the one-kernel plan only
     if (!idx_in) {
         RouteArgs r = route_args(L, x, ws, o, idx_out, w_out, nullptr, nullptr, nullptr);
         const int st = cuda_status(launch_route_topk(r, 1, s, true));
@@ -295,6 +300,7 @@ int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_de
         if (st != SMOE_OK) return st;
         if (L.d_model != L0.d_model || L.n_experts != L0.n_experts || L.top_k != L0.top_k ||
             L.ffn_dim != L0.ffn_dim || L.norm_topk_prob != L0.norm_topk_prob ||
+            is_q2(L) != is_q2(L0) ||
             (L.rms_gain == nullptr) != (L0.rms_gain == nullptr) || L.rms_eps != L0.rms_eps)
             return SMOE_ERR_INVALID_ARG;
         const void *ptrs[] = {L.router_w, L.gate_q, L.gate_s, L.gate_b, L.up_q, L.up_s, L.up_b,
@@ -332,6 +338,7 @@ int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_de
         f.n_layers = n_layers;
         f.act0 = act[0];
         f.act1 = act[1];
+        f.q2 = is_q2(L0) ? 1 : 0;
         if (fused_plan(f, device_sm_count())) return cuda_status(launch_decode_layer(f, s, true));
     }
     // one launch sequence per layer, activations ping-ponging in the workspace
@@ -353,6 +360,7 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     if (st != SMOE_OK) return st;
     if (!x || !y || T < 1 || T > kMaxChunk || !aligned(x, 16) || !aligned(y, 16) || x == y)
         return SMOE_ERR_INVALID_ARG;
+    if (is_q2(*layer)) return SMOE_ERR_UNSUPPORTED;           // Q2 prefill is not built
     if ((st = check_ws(layer, T, ws, ws_bytes)) != SMOE_OK) return st;
     const smoe_layer &L = *layer;
     const WsLayout o = ws_layout(L, T);
@@ -415,7 +423,17 @@ int smoe_quantize_q4(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smo
     if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scale, 2) || !aligned(bias, 2))
         return SMOE_ERR_INVALID_ARG;
     const long long n_groups = (long long)rows * (cols / kGroup);
-    return cuda_status(launch_quantize_q4(w, n_groups, codes, scale, bias, (cudaStream_t)stream));
+    return cuda_status(launch_quantize(w, n_groups, 4, codes, scale, bias, (cudaStream_t)stream));
+}
+
+int smoe_quantize_q2(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smoe_bf16 *scale,
+                     smoe_bf16 *bias, smoe_stream stream) {
+    if (!w || !codes || !scale || !bias || rows < 1 || cols < 1) return SMOE_ERR_INVALID_ARG;
+    if (cols % kGroup) return SMOE_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scale, 2) || !aligned(bias, 2))
+        return SMOE_ERR_INVALID_ARG;
+    const long long n_groups = (long long)rows * (cols / kGroup);
+    return cuda_status(launch_quantize(w, n_groups, 2, codes, scale, bias, (cudaStream_t)stream));
 }
 
 const char *smoe_status_string(int status) {

@@ -150,6 +150,37 @@ __device__ __forceinline__ float dot32(uint4 c, const float4 (&x)[8]) {
     return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
+// SMOE-Q2: sum_k (128+q_k) x_k over the 32 codes of an 8-byte chunk.  In a
+// 32-bit word, element 4j+k sits in bits 2k..2k+1 of byte j: the mask
+// (w >> 2k) & 0x03030303 holds elements k, 4+k, 8+k, 12+k one per byte, and
+// the byte permute turns each into the float 128 + q exactly.
+__device__ __forceinline__ void dot16q2(uint32_t w, const float4 *x, float2 &a0, float2 &a1) {
+    const uint32_t t0 = w & 0x03030303u, t1 = (w >> 2) & 0x03030303u;
+    const uint32_t t2 = (w >> 4) & 0x03030303u, t3 = (w >> 6) & 0x03030303u;
+    a0 = ffma2(make_float2(code_f32<0>(t0), code_f32<0>(t1)), make_float2(x[0].x, x[0].y), a0);
+    a1 = ffma2(make_float2(code_f32<0>(t2), code_f32<0>(t3)), make_float2(x[0].z, x[0].w), a1);
+    a0 = ffma2(make_float2(code_f32<1>(t0), code_f32<1>(t1)), make_float2(x[1].x, x[1].y), a0);
+    a1 = ffma2(make_float2(code_f32<1>(t2), code_f32<1>(t3)), make_float2(x[1].z, x[1].w), a1);
+    a0 = ffma2(make_float2(code_f32<2>(t0), code_f32<2>(t1)), make_float2(x[2].x, x[2].y), a0);
+    a1 = ffma2(make_float2(code_f32<2>(t2), code_f32<2>(t3)), make_float2(x[2].z, x[2].w), a1);
+    a0 = ffma2(make_float2(code_f32<3>(t0), code_f32<3>(t1)), make_float2(x[3].x, x[3].y), a0);
+    a1 = ffma2(make_float2(code_f32<3>(t2), code_f32<3>(t3)), make_float2(x[3].z, x[3].w), a1);
+}
+
+// The 32-code chunk at p (16 bytes of Q4 codes, or 8 of Q2) against x.
+template <bool kQ2>
+__device__ __forceinline__ float dot_chunk(const unsigned char *p, const float4 (&x)[8]) {
+    if constexpr (kQ2) {
+        const uint2 c = *reinterpret_cast<const uint2 *>(p);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+        dot16q2(c.x, x, a0, a1);
+        dot16q2(c.y, x + 4, a0, a1);
+        return (a0.x + a0.y) + (a1.x + a1.y);
+    } else {
+        return dot32(*reinterpret_cast<const uint4 *>(p), x);
+    }
+}
+
 // Warp-wide sums of eight values at once (v[j] of every lane): 9 shuffles
 // instead of 40.  Each exchange halves the values a lane carries; lane L ends
 // with the total of v[4*b4 + 2*b3 + b2] (b = bits of L), held by 4 lanes.
@@ -213,8 +244,9 @@ __device__ __forceinline__ LW layer_w(const FusedArgs &a, int l) {
 
 // ---------------------------------------------------------------- kernel
 
-template <bool kRoute>
+template <bool kRoute, bool kQ2>
 __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
+    constexpr int kCB = kQ2 ? 8 : 16;            // bytes of a 32-code chunk
     extern __shared__ __align__(128) unsigned char sm[];
     const int D = a.D, F = a.F, K = a.K, E = a.E;
     const int NC = D / 32;                       // 32-code chunks of a gate/up row
@@ -285,7 +317,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             const int i = p / F, j0 = p - i * F, n = min(a.r_gu, min(p1 - p, F - j0));
             const uint32_t s = g % kSlots;
             unsigned char *dst = ring + s * a.slot_bytes;
-            const uint32_t cb = n * (D / 2), sb = n * NG * 2;
+            const uint32_t cb = n * (D / 32 * kCB), sb = n * NG * 2;
             if (lane == 0) {
                 mb_wait(&empty[s], ((g / kSlots) & 1) ^ 1, a.status);
                 mb_expect(&full[s], 2 * cb + 4 * sb);
@@ -294,7 +326,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
             const size_t row = (size_t)__shfl_sync(0xffffffffu, my_e, i) * F + j0;
             if (lane < 2) {
-                bulk_g2s(dst + lane * cb, (lane ? W.uq : W.gq) + row * (D / 2), cb, &full[s]);
+                bulk_g2s(dst + lane * cb, (lane ? W.uq : W.gq) + row * (D / 32 * kCB), cb, &full[s]);
             } else if (lane < 6) {
                 const uint16_t *src = lane == 2 ? W.gs : lane == 3 ? W.gb : lane == 4 ? W.us : W.ub;
                 bulk_g2s(dst + 2 * cb + (lane - 2) * sb, src + row * NG, sb, &full[s]);
@@ -305,7 +337,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             const int nr = min(a.dn_nr, rows - r0);
             const uint32_t s = g % kSlots;
             unsigned char *dst = ring + s * a.slot_bytes;
-            const uint32_t cb = nr * (F / 2), sb = nr * FG * 2;
+            const uint32_t cb = nr * (F / 32 * kCB), sb = nr * FG * 2;
             if (lane == 0) {
                 mb_wait(&empty[s], ((g / kSlots) & 1) ^ 1, a.status);
                 mb_expect(&full[s], K * (cb + 2 * sb));
@@ -318,7 +350,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 const int i = q % K, kind = q / K;
                 const size_t row = (size_t)(q < 32 ? e_lo : e_hi) * D + d0 + r0;
                 if (kind == 0)
-                    bulk_g2s(dst + i * cb, W.dq + row * (F / 2), cb, &full[s]);
+                    bulk_g2s(dst + i * cb, W.dq + row * (F / 32 * kCB), cb, &full[s]);
                 else
                     bulk_g2s(dst + K * cb + ((kind - 1) * K + i) * sb, (kind == 1 ? W.ds : W.db) + row * FG, sb,
                              &full[s]);
@@ -575,15 +607,14 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             const uint32_t s = g % kSlots;
             warp_wait(&full[s], (g / kSlots) & 1, a.status);
             const unsigned char *slot = ring + s * a.slot_bytes;
-            const uint32_t cb = n * (D / 2);
+            const uint32_t RBg = D / 32 * kCB, cb = n * RBg;
             const uint16_t *gsr = reinterpret_cast<const uint16_t *>(slot + 2 * cb);
             const uint16_t *gbr = gsr + n * NG, *usr = gbr + n * NG, *ubr = usr + n * NG;
             for (int r = rs; r < n; r += rstep) {
                 float ag = 0.f, au = 0.f;
                 if (ca < NC) {
-                    const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r * (D / 2) + ca * 16);
-                    const uint4 cu = *reinterpret_cast<const uint4 *>(slot + cb + r * (D / 2) + ca * 16);
-                    const float A = dot32(cg, xa), B = dot32(cu, xa);
+                    const float A = dot_chunk<kQ2>(slot + r * RBg + ca * kCB, xa);
+                    const float B = dot_chunk<kQ2>(slot + cb + r * RBg + ca * kCB, xa);
                     const int gi = r * NG + (ca >> 1);
                     const float s0 = bf16_to_f32(gsr[gi]), b0 = bf16_to_f32(gbr[gi]);
                     const float s1 = bf16_to_f32(usr[gi]), b1 = bf16_to_f32(ubr[gi]);
@@ -591,9 +622,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                     au = s1 * B + (b1 - 128.f * s1) * Xa;
                 }
                 if (cbk < NC) {
-                    const uint4 cg = *reinterpret_cast<const uint4 *>(slot + r * (D / 2) + cbk * 16);
-                    const uint4 cu = *reinterpret_cast<const uint4 *>(slot + cb + r * (D / 2) + cbk * 16);
-                    const float A = dot32(cg, xb), B = dot32(cu, xb);
+                    const float A = dot_chunk<kQ2>(slot + r * RBg + cbk * kCB, xb);
+                    const float B = dot_chunk<kQ2>(slot + cb + r * RBg + cbk * kCB, xb);
                     const int gi = r * NG + (cbk >> 1);
                     const float s0 = bf16_to_f32(gsr[gi]), b0 = bf16_to_f32(gbr[gi]);
                     const float s1 = bf16_to_f32(usr[gi]), b1 = bf16_to_f32(ubr[gi]);
@@ -676,16 +706,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             if (real) warp_wait(&full[s], (g / kSlots) & 1, a.status);
             const unsigned char *slot = ring + (real ? s : 0) * a.slot_bytes;
             if (dn_live && sp < nr) {
-                const uint32_t cb = nr * (F / 2), sb = nr * FG * 2;
-                const unsigned char *cp = slot + di * cb + dc * 16;
+                const uint32_t cb = nr * (F / 32 * kCB), sb = nr * FG * 2;
+                const unsigned char *cp = slot + di * cb + dc * kCB;
                 const uint16_t *sp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + di * sb) + (dc >> 1);
                 const uint16_t *bp16 = reinterpret_cast<const uint16_t *>(slot + K * cb + (K + di) * sb) + (dc >> 1);
                 float acc[kDnU];
 #pragma unroll
                 for (int u = 0; u < kDnU; ++u) {
                     const int rr = min(sp + u * RS, nr - 1);          // a row past the item repeats the last
-                    const uint4 cv = *reinterpret_cast<const uint4 *>(cp + rr * (F / 2));
-                    const float A = dot32(cv, hq);
+                    const float A = dot_chunk<kQ2>(cp + rr * (F / 32 * kCB), hq);
                     const float sc = bf16_to_f32(sp16[rr * FG]), bi = bf16_to_f32(bp16[rr * FG]);
                     acc[u] = sc * A + (bi - 128.f * sc) * Hc;
                 }
@@ -745,8 +774,9 @@ bool fused_plan(FusedArgs &a, int num_sms) {
     a.dn_gran = gran;
     const int units = D / gran;
     a.rows_max = ((units + a.grid - 1) / a.grid) * gran;
-    const int row_pair_bytes = 2 * (D / 2 + NG * 2 * 2);
-    const int dn_row_bytes = K * (F / 2 + FG * 2 * 2);       // one down row, all K slots
+    const int cb32 = a.q2 ? 8 : 16;                           // bytes of a 32-code chunk
+    const int row_pair_bytes = 2 * (D / 32 * cb32 + NG * 2 * 2);
+    const int dn_row_bytes = K * (F / 32 * cb32 + FG * 2 * 2);  // one down row, all K slots
     // gate/up: one row pair per (group of NCP warps) per item
     const int NCPh = (D / 32 + 63) / 64;
     a.r_gu = kWarpsC / NCPh;
@@ -772,23 +802,22 @@ bool fused_plan(FusedArgs &a, int num_sms) {
 // Floats of h scratch the fused kernel needs (its padded down-phase layout).
 size_t fused_h_floats(int F, int K) { return (size_t)K * ((F / 32 + 7) / 8) * 256; }
 
-cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route) {
-    static int attr[2] = {0, 0};
+template <bool kRoute, bool kQ2>
+static cudaError_t launch_variant(const FusedArgs &a, cudaStream_t s) {
+    static int attr = 0;                      // dynamic shared memory already allowed
     const size_t smem = a.smem_bytes;
-    if (route) {
-        if (attr[1] < (int)smem) {
-            cudaError_t e = cudaFuncSetAttribute(k_decode_layer<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            attr[1] = (int)smem;
-        }
-        return launch_kernel(k_decode_layer<true>, dim3(a.grid), dim3(kThreadsF), smem, s, true, a);
-    }
-    if (attr[0] < (int)smem) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_layer<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr < (int)smem) {
+        cudaError_t e = cudaFuncSetAttribute(k_decode_layer<kRoute, kQ2>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr[0] = (int)smem;
+        attr = (int)smem;
     }
-    return launch_kernel(k_decode_layer<false>, dim3(a.grid), dim3(kThreadsF), smem, s, true, a);
+    return launch_kernel(k_decode_layer<kRoute, kQ2>, dim3(a.grid), dim3(kThreadsF), smem, s, true, a);
+}
+
+cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route) {
+    if (a.q2) return route ? launch_variant<true, true>(a, s) : launch_variant<false, true>(a, s);
+    return route ? launch_variant<true, false>(a, s) : launch_variant<false, false>(a, s);
 }
 
 }  // namespace smoe

@@ -158,7 +158,6 @@ constexpr int kQWarps = 4;
 constexpr int kQThreads = kQWarps * 32;
 constexpr int kQCtasPerSm = 4;
 constexpr int kQStages = 3;                              // 4 KiB stages per warp
-constexpr uint32_t kQPackBias = 0xFB000000u;            // 0x4B000000 * 0x11111111 mod 2^32
 
 // 16-byte asynchronous copy global -> shared (L2 only); src_bytes = 0 fills
 // the 16 bytes with zeros without reading.
@@ -190,14 +189,19 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return *reinterpret_cast<float2 *>(&rd);
 }
 
-// The codes of one group of 64 weights (32 bf16 pairs in u), its scale and
-// bias.  Code q = the integer nearest (halves to even) to d * r, d = RN(w - mn),
-// r = RN(1 / scale), the product exact: one fused multiply-add d * r + 2^23
-// rounds it once, onto the integers, leaving 0x4B000000 + q as its bits.
-// Eight such words e_k combine into the code word sum_k q_k 16^k as
-// (sum_k e_k 16^k) - 0x4B000000 * 0x11111111 (mod 2^32), one shift-add each.
-__device__ __forceinline__ void q4_group(const uint32_t (&u)[32], uint32_t (&code)[8], uint16_t &sb,
-                                         uint16_t &bb) {
+// The codes (kBits = 4: SMOE-Q4, 2: SMOE-Q2) of one group of 64 weights (32
+// bf16 pairs in u), its scale and bias.  Code q = the integer nearest (halves
+// to even) to d * r, d = RN(w - mn), r = RN(1 / scale), the product exact: one
+// fused multiply-add d * r + 2^23 rounds it once, onto the integers, leaving
+// 0x4B000000 + q as its bits.  The n = 32 / kBits such words e_k of a code
+// word combine into sum_k q_k 2^(kBits k) as (sum_k e_k 2^(kBits k)) minus
+// 0x4B000000 * sum_k 2^(kBits k) (mod 2^32), one shift-add each.
+template <int kBits>
+__device__ __forceinline__ void q_group(const uint32_t (&u)[32], uint32_t (&code)[2 * kBits], uint16_t &sb,
+                                        uint16_t &bb) {
+    constexpr int kWords = 2 * kBits, kPairs = 16 / kBits;  // code words; bf16 pairs per code word
+    constexpr uint32_t kPackBias = kBits == 4 ? 0xFB000000u : 0xE7000000u;   // 0x4B000000 * 0x11111111 / 0x55555555
+    constexpr float kLevels = (float)((1 << kBits) - 1);
     uint32_t mn2 = u[0], mx2 = u[0];
 #pragma unroll
     for (int k = 1; k < 32; ++k) {
@@ -206,12 +210,12 @@ __device__ __forceinline__ void q4_group(const uint32_t (&u)[32], uint32_t (&cod
     }
     const float mn = fminf(__uint_as_float(mn2 << 16), __uint_as_float(mn2 & 0xFFFF0000u));
     const float mx = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
-    sb = f32_to_bf16(__fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), 15.0f));
+    sb = f32_to_bf16(__fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), kLevels));
     bb = f32_to_bf16(__fadd_rn(mn, 0.0f));
     const float s = bf16_to_f32(sb);
     if (s == 0.0f) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) code[k] = 0u;
+        for (int k = 0; k < kWords; ++k) code[k] = 0u;
         return;
     }
     if (s >= 0x1p-126f) {
@@ -219,27 +223,27 @@ __device__ __forceinline__ void q4_group(const uint32_t (&u)[32], uint32_t (&cod
         const float2 mn_2 = make_float2(mn, mn), r_2 = make_float2(r, r);
         const float2 m23 = make_float2(8388608.0f, 8388608.0f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kWords; ++k) {
             uint32_t acc = 0;
 #pragma unroll
-            for (int j = 3; j >= 0; --j) {                  // elements 8k+2j+1, 8k+2j, highest first
-                const uint32_t p = u[4 * k + j];
+            for (int j = kPairs - 1; j >= 0; --j) {         // elements 2j+1, 2j of the word, highest first
+                const uint32_t p = u[kPairs * k + j];
                 const float2 d = fsub2(make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)), mn_2);
                 const float2 c = ffma2(d, r_2, m23);
-                acc = (acc << 4) + __float_as_uint(c.y);
-                acc = (acc << 4) + __float_as_uint(c.x);
+                acc = (acc << kBits) + __float_as_uint(c.y);
+                acc = (acc << kBits) + __float_as_uint(c.x);
             }
-            code[k] = acc - kQPackBias;
+            code[k] = acc - kPackBias;
         }
     } else {                                                 // scale below binary32's normal range
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kWords; ++k) {
             uint32_t acc = 0;
 #pragma unroll
-            for (int e = 7; e >= 0; --e) {
-                const uint32_t p = u[4 * k + (e >> 1)];
+            for (int e = 2 * kPairs - 1; e >= 0; --e) {
+                const uint32_t p = u[kPairs * k + (e >> 1)];
                 const float w = __uint_as_float((e & 1) ? (p & 0xFFFF0000u) : (p << 16));
-                acc = (acc << 4) + (uint32_t)rintf(__fdiv_rn(__fsub_rn(w, mn), s));
+                acc = (acc << kBits) + (uint32_t)rintf(__fdiv_rn(__fsub_rn(w, mn), s));
             }
             code[k] = acc;
         }
@@ -252,9 +256,10 @@ __device__ __forceinline__ void q4_group(const uint32_t (&u)[32], uint32_t (&cod
 // copies chunks l + 32 j: coalesced), kQStages - 1 steps ahead; chunk c of
 // group g sits at g*128 + ((c ^ g) & 7)*16, so the 8 lanes of a read phase
 // each take a different 16-byte bank group.
+template <int kBits>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
-    k_quantize_q4(const uint16_t *__restrict__ w, long long n_groups, uint8_t *__restrict__ codes,
-                  uint16_t *__restrict__ scale, uint16_t *__restrict__ bias) {
+    k_quantize(const uint16_t *__restrict__ w, long long n_groups, uint8_t *__restrict__ codes,
+               uint16_t *__restrict__ scale, uint16_t *__restrict__ bias) {
     __shared__ __align__(16) unsigned char ring[kQWarps][kQStages][4096];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long warps = (long long)gridDim.x * kQWarps;
@@ -291,13 +296,14 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         }
         __syncwarp();                                        // stage read: free to be refilled
         const long long grp = (st0 + i * warps) * 32 + lane;
-        uint32_t code[8];
+        uint32_t code[2 * kBits];
         uint16_t sb, bb;
-        q4_group(u, code, sb, bb);
+        q_group<kBits>(u, code, sb, bb);
         if (grp < n_groups) {
-            uint4 *cq = reinterpret_cast<uint4 *>(codes + grp * 32);
-            cq[0] = make_uint4(code[0], code[1], code[2], code[3]);
-            cq[1] = make_uint4(code[4], code[5], code[6], code[7]);
+            uint4 *cq = reinterpret_cast<uint4 *>(codes + grp * (8 * kBits));
+#pragma unroll
+            for (int k = 0; k < kBits / 2; ++k)
+                cq[k] = make_uint4(code[4 * k], code[4 * k + 1], code[4 * k + 2], code[4 * k + 3]);
             scale[grp] = sb;
             bias[grp] = bb;
         }
@@ -316,13 +322,16 @@ cudaError_t launch_dense_matvec(const uint16_t *w, const uint16_t *x, int rows, 
     return launch_mv_rb<1>(w, x, rows, cols, y, cap, s);
 }
 
-cudaError_t launch_quantize_q4(const uint16_t *w, long long n_groups, uint8_t *codes, uint16_t *scale,
-                               uint16_t *bias, cudaStream_t s) {
+cudaError_t launch_quantize(const uint16_t *w, long long n_groups, int bits, uint8_t *codes, uint16_t *scale,
+                            uint16_t *bias, cudaStream_t s) {
     const long long steps = (n_groups + 31) / 32;
     const long long need = (steps + kQWarps - 1) / kQWarps;
     const long long cap = (long long)device_sm_count() * kQCtasPerSm;
     const int grid = (int)(need < cap ? need : cap);
-    k_quantize_q4<<<grid, kQThreads, 0, s>>>(w, n_groups, codes, scale, bias);
+    if (bits == 2)
+        k_quantize<2><<<grid, kQThreads, 0, s>>>(w, n_groups, codes, scale, bias);
+    else
+        k_quantize<4><<<grid, kQThreads, 0, s>>>(w, n_groups, codes, scale, bias);
     return cudaGetLastError();
 }
 

@@ -12,10 +12,11 @@ namespace smoe {
 cudaError_t launch_dense_matvec(const uint16_t *w, const uint16_t *x, int rows, int cols, float *y,
                                 cudaStream_t s);
 
-// Codes, scales and biases of n_groups consecutive groups of 64 bf16 weights
-// (w and codes 16-byte aligned, scale and bias 2-byte aligned).
-cudaError_t launch_quantize_q4(const uint16_t *w, long long n_groups, uint8_t *codes, uint16_t *scale,
-                               uint16_t *bias, cudaStream_t s);
+// SMOE-Q4 (bits 4) or SMOE-Q2 (bits 2) codes, scales and biases of n_groups
+// consecutive groups of 64 bf16 weights (w and codes 16-byte aligned, scale
+// and bias 2-byte aligned).
+cudaError_t launch_quantize(const uint16_t *w, long long n_groups, int bits, uint8_t *codes, uint16_t *scale,
+                            uint16_t *bias, cudaStream_t s);
 
 int device_sm_count();
 

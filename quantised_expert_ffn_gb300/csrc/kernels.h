@@ -101,6 +101,7 @@ struct FusedArgs {
     const smoe_layer *layers;   // stack variant: device table of n_layers layers (NULL: the pointers above)
     int n_layers;               // layers run by one launch (1 unless `layers` is set)
     uint16_t *act0, *act1;      // stack variant: [D] bf16 activations between layers (ping-pong)
+    int q2;                     // 1: SMOE-Q2 codes (2 bits, 8 bytes per 32 codes), 0: SMOE-Q4
     // plan (fused_plan)
     int grid, r_gu, dn_nr, dn_gran, dn_rs, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
 };

@@ -53,6 +53,7 @@ class smoe_layer(ctypes.Structure):
         ("down_q", ctypes.c_void_p),
         ("down_s", ctypes.c_void_p),
         ("down_b", ctypes.c_void_p),
+        ("code_bits", ctypes.c_int),
     ]
 
 
@@ -77,6 +78,7 @@ def _load():
         "smoe_last_cuda_error": (ctypes.c_char_p, []),
         "smoe_dense_matvec": (I, [P, P, I, I, P, P]),
         "smoe_quantize_q4": (I, [P, I, I, P, P, P, P]),
+        "smoe_quantize_q2": (I, [P, I, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -89,7 +91,8 @@ _lib = _load()
 EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_status",
             "smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_ffn_decode",
             "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc",
-            "smoe_last_cuda_error", "smoe_moe_decode_layers", "smoe_dense_matvec", "smoe_quantize_q4")
+            "smoe_last_cuda_error", "smoe_moe_decode_layers", "smoe_dense_matvec", "smoe_quantize_q4",
+            "smoe_quantize_q2")
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -128,6 +131,7 @@ class Layer:
         s.norm_topk_prob = int(bool(w.norm_topk_prob))
         s.rms_eps = float(w.rms_eps)
         s.rms_gain = None if w.rms_gain is None else w.rms_gain.data_ptr()
+        s.code_bits = int(getattr(w, "code_bits", 4))
         for n in ("router_w", "gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q",
                   "down_s", "down_b"):
             t = getattr(w, n)
@@ -208,6 +212,16 @@ def smoe_quantize_q4(w, codes, scale, bias, stream=None):
     _check(_lib.smoe_quantize_q4(_p(w), int(rows), int(cols), _p(codes), _p(scale), _p(bias),
                                  _stream(stream)),
            "smoe_quantize_q4")
+
+
+def smoe_quantize_q2(w, codes, scale, bias, stream=None):
+    """SMOE-Q2 of bf16 weights w [..., cols]: codes uint8 [..., cols/4], scale and
+    bias bf16 [..., cols/64]."""
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    _check(_lib.smoe_quantize_q2(_p(w), int(rows), int(cols), _p(codes), _p(scale), _p(bias),
+                                 _stream(stream)),
+           "smoe_quantize_q2")
 
 
 SMOE_DECODE_NOALLOC_MAX_BYTES = 512 * 1024

@@ -154,6 +154,21 @@ def test_dense_matvec_and_quantiser_reject_bad_arguments_on_host(lib):
     assert qz(w=P((1 << 20) + 2)) == lib.SMOE_ERR_INVALID_ARG
     assert qz(c=P((1 << 23) + 8)) == lib.SMOE_ERR_INVALID_ARG              # codes not 16-byte aligned
     assert qz(s=P((1 << 24) + 1)) == lib.SMOE_ERR_INVALID_ARG
+    q2 = lambda cols=2048, c=C: so.smoe_quantize_q2(W, 768, cols, c, S, B, None)
+    assert q2(cols=96) == lib.SMOE_ERR_UNSUPPORTED
+    assert q2(c=P((1 << 23) + 4)) == lib.SMOE_ERR_INVALID_ARG
+    assert q2(c=None) == lib.SMOE_ERR_INVALID_ARG
+
+
+def test_layer_code_bits_checked_on_host(lib):
+    so = lib._lib
+    P = ctypes.c_void_p
+    ws = P(1 << 24)
+    for bits, want in ((3, lib.SMOE_ERR_UNSUPPORTED), (8, lib.SMOE_ERR_UNSUPPORTED)):
+        L = _layer(lib)
+        L.code_bits = bits
+        assert so.smoe_workspace_bytes(ctypes.byref(L), 1) == 0
+        assert so.smoe_moe_decode(ctypes.byref(L), P(4096), P(8192), None, None, None, ws, 1 << 30, None) == want
 
 
 def test_status_strings(lib):
