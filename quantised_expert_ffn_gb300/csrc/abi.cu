@@ -360,9 +360,10 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     if (st != SMOE_OK) return st;
     if (!x || !y || T < 1 || T > kMaxChunk || !aligned(x, 16) || !aligned(y, 16) || x == y)
         return SMOE_ERR_INVALID_ARG;
-    if (is_q2(*layer)) return SMOE_ERR_UNSUPPORTED;           // Q2 prefill is not built
     if ((st = check_ws(layer, T, ws, ws_bytes)) != SMOE_OK) return st;
     const smoe_layer &L = *layer;
+    const bool tc = prefill_path() == 1 && prefill_tc_supported(L.d_model, L.ffn_dim);
+    if (is_q2(L) && !tc) return SMOE_ERR_UNSUPPORTED;        // Q2 runs on the tensor-core path only
     const WsLayout o = ws_layout(L, T);
     cudaStream_t s = (cudaStream_t)stream;
     int32_t *idx = idx_out_opt ? idx_out_opt : at<int32_t>(ws, o.idx);
@@ -399,7 +400,8 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     p.y = y;
     p.status = at<int32_t>(ws, o.status);
     p.num_sms = device_sm_count();
-    if (prefill_path() == 1 && prefill_tc_supported(p.D, p.F)) {
+    p.q2 = is_q2(L) ? 1 : 0;
+    if (tc) {
         if ((st = cuda_status(launch_prefill_tc(p, s))) != SMOE_OK) return st;
         return cuda_status(launch_prefill_combine(p, s, true));
     }

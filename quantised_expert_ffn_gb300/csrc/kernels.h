@@ -128,6 +128,7 @@ struct PrefillArgs {
     uint16_t *y;                // [T][D]
     int32_t *status;
     int num_sms;
+    int q2;                     // 1: SMOE-Q2 codes (tensor-core path only)
 };
 // CUDA-core path: gate/up, down and combine (fp32 h)
 cudaError_t launch_prefill_simt(const PrefillArgs &a, const uint16_t *xn, float *h32, cudaStream_t s,

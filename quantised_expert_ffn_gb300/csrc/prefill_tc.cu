@@ -241,6 +241,30 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2,
     }
 }
 
+// SMOE-Q2: the 16 codes of one word (element e in bits 2e) -> 8 half2, in the
+// order dequant_word gives a Q4 word's 8 elements -- (e_i, e_{i+4}) of the
+// block of elements 0-7 (o0), then of 8-15 (o1) -- so the activation side
+// keeps its permutation.  A byte permute puts bytes 0 and 1 (elements 0-3,
+// 4-7) into the two half-words of one register, bytes 2 and 3 into another;
+// each 2-bit field then becomes the fp16 1024 + q exactly, as for Q4.
+__device__ __forceinline__ void dequant_word_q2(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o0)[4],
+                                                uint32_t (&o1)[4]) {
+    const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(lo) : "r"(w));    // [b0, 0, b1, 0]
+    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(hi) : "r"(w));    // [b2, 0, b3, 0]
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t m0, m1;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(m0) : "r"(lo >> (2 * i)), "r"(0x00030003u), "r"(0x64006400u));
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(m1) : "r"(hi >> (2 * i)), "r"(0x00030003u), "r"(0x64006400u));
+        __half2 v0 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&m0), k1024), s2, b2);
+        __half2 v1 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&m1), k1024), s2, b2);
+        o0[i] = *reinterpret_cast<uint32_t *>(&v0);
+        o1[i] = *reinterpret_cast<uint32_t *>(&v1);
+    }
+}
+
 __device__ __forceinline__ int perm8(int f) {   // position of element f in the permuted order
     const int i = f & 7;
     return (f & ~7) | (i < 4 ? 2 * i : 2 * (i - 4) + 1);
@@ -255,7 +279,7 @@ struct Smem {
     static constexpr int kBytes = kBarOff + 1024;   // barriers + tmem slot + flags
 };
 
-template <bool kPair>
+template <bool kPair, bool kQ2>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
@@ -329,9 +353,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t ph = (g / kStages) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
                     unsigned char *stg = st_ring + s * S::kStageBytes;
-                    mbar_expect_tx(&full[s], S::kMats * kCodeBytes + bbytes);
-                    tma_load_2d(stg, &tm_a0, c * (kKc / 2), row, &full[s]);
-                    if (kPair) tma_load_2d(stg + kCodeBytes, &tm_a1, c * (kKc / 2), row, &full[s]);
+                    constexpr int kCodeRow = kQ2 ? kKc / 4 : kKc / 2;   // code bytes of a row's chunk
+                    mbar_expect_tx(&full[s], S::kMats * kTile * kCodeRow + bbytes);
+                    tma_load_2d(stg, &tm_a0, c * kCodeRow, row, &full[s]);
+                    if (kPair) tma_load_2d(stg + kCodeBytes, &tm_a1, c * kCodeRow, row, &full[s]);
                     tma_load_2d(stg + S::kMats * kCodeBytes, tb, c * kKc, off, &full[s]);
                 }
             }
@@ -439,20 +464,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 const unsigned char *stg = st_ring + s * S::kStageBytes;
-                const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 32 + h * 16);
-                uint4 c1 = c0;
-                if (kPair) c1 = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + h * 16);
-                mbar_arrive(&empty[s]);                   // codes consumed
                 uint32_t q0[4][4], q1[4][4];
-                dequant_word(c0.x, s0, b0, q0[0]);
-                dequant_word(c0.y, s0, b0, q0[1]);
-                dequant_word(c0.z, s0, b0, q0[2]);
-                dequant_word(c0.w, s0, b0, q0[3]);
-                if (kPair) {
-                    dequant_word(c1.x, s1, b1, q1[0]);
-                    dequant_word(c1.y, s1, b1, q1[1]);
-                    dequant_word(c1.z, s1, b1, q1[2]);
-                    dequant_word(c1.w, s1, b1, q1[3]);
+                if constexpr (kQ2) {                      // 16 bytes per row: half h = 8 bytes, two words
+                    const uint2 c0 = *reinterpret_cast<const uint2 *>(stg + r * 16 + h * 8);
+                    uint2 c1 = c0;
+                    if (kPair) c1 = *reinterpret_cast<const uint2 *>(stg + kCodeBytes + r * 16 + h * 8);
+                    mbar_arrive(&empty[s]);               // codes consumed
+                    dequant_word_q2(c0.x, s0, b0, q0[0], q0[1]);
+                    dequant_word_q2(c0.y, s0, b0, q0[2], q0[3]);
+                    if (kPair) {
+                        dequant_word_q2(c1.x, s1, b1, q1[0], q1[1]);
+                        dequant_word_q2(c1.y, s1, b1, q1[2], q1[3]);
+                    }
+                } else {
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 32 + h * 16);
+                    uint4 c1 = c0;
+                    if (kPair) c1 = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + h * 16);
+                    mbar_arrive(&empty[s]);               // codes consumed
+                    dequant_word(c0.x, s0, b0, q0[0]);
+                    dequant_word(c0.y, s0, b0, q0[1]);
+                    dequant_word(c0.z, s0, b0, q0[2]);
+                    dequant_word(c0.w, s0, b0, q0[3]);
+                    if (kPair) {
+                        dequant_word(c1.x, s1, b1, q1[0]);
+                        dequant_word(c1.y, s1, b1, q1[1]);
+                        dequant_word(c1.z, s1, b1, q1[2]);
+                        dequant_word(c1.w, s1, b1, q1[3]);
+                    }
                 }
                 tc_fence_after();      // A stage a: its last MMAs completed before these codes landed
                 const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols + h * 16;
@@ -575,7 +613,7 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kPair>
+template <bool kPair, bool kQ2>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap (&b)[4],
                       const TcParams &p, cudaStream_t s, int grid) {
     // More than half of an SM's shared memory: one CTA per SM.  Two resident
@@ -584,11 +622,11 @@ cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtens
     const size_t smem = std::max<size_t>(Smem<kPair>::kBytes + 1024, 120 * 1024);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<kPair, kQ2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_kernel(k_prefill_tc<kPair>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
+    return launch_kernel(k_prefill_tc<kPair, kQ2>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
                          b[1], b[2], b[3], p);
 }
 
@@ -599,12 +637,13 @@ bool prefill_tc_supported(int D, int F) { return D % kTile == 0 && F % kTile == 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     const int TK = a.T * a.K;
     CUtensorMap mg, mu, md, mx[4], mh[4];
-    bool ok = make_map(&mg, a.gq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / 2, (uint64_t)a.E * a.F, kKc / 2, kTile,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&mu, a.uq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / 2, (uint64_t)a.E * a.F, kKc / 2, kTile,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&md, a.dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.F / 2, (uint64_t)a.E * a.D, kKc / 2, kTile,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int per_byte = a.q2 ? 4 : 2;                    // codes per byte
+    bool ok = make_map(&mg, a.gq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / per_byte, (uint64_t)a.E * a.F,
+                       kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&mu, a.uq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / per_byte, (uint64_t)a.E * a.F,
+                       kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&md, a.dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.F / per_byte, (uint64_t)a.E * a.D,
+                       kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
     for (int i = 0; i < 4 && ok; ++i)
         ok = make_map(&mx[i], a.xperm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.D, TK, kKc, 16 * (i + 1),
                       CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -629,7 +668,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     gu.vec_scales = (a.D / kGroup) % 8 == 0 && a16(a.gs) && a16(a.gb) && a16(a.us) && a16(a.ub);
     gu.hout = a.hbuf;
     gu.status = a.status;
-    if ((e = launch_tc<true>(mg, mu, mx, gu, s, grid)) != cudaSuccess) return e;
+    if ((e = a.q2 ? launch_tc<true, true>(mg, mu, mx, gu, s, grid) : launch_tc<true, false>(mg, mu, mx, gu, s, grid)) !=
+        cudaSuccess)
+        return e;
     TcParams dn = gu;
     dn.n_tiles = a.D / kTile;
     dn.n_chunks = a.F / kKc;
@@ -640,7 +681,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     dn.vec_scales = (a.F / kGroup) % 8 == 0 && a16(a.ds) && a16(a.db);
     dn.hout = nullptr;
     dn.oout = a.obuf;
-    return launch_tc<false>(md, md, mh, dn, s, grid);
+    return a.q2 ? launch_tc<false, true>(md, md, mh, dn, s, grid) : launch_tc<false, false>(md, md, mh, dn, s, grid);
 }
 
 }  // namespace smoe

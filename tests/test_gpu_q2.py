@@ -115,16 +115,41 @@ def test_q2_decode_layers_equals_chained(smoe, name, n):
     assert smoe.smoe_read_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("name,T,alpha", [("f512", 8, None), ("30b", 45, None), ("235b", 64, 0.7),
+                                          ("f1536", 5, None)])
+def test_q2_prefill_chunk_against_oracle(smoe, orc, name, T, alpha):
+    """Q2 prefill on the tensor cores (the Q2 dequant feeds A in the Q4 element
+    order): ids bit-exact, values within 2e-3 of the oracle."""
+    W, OL = q2_layer(name, seed=11)
+    K = W.top_k
+    x = margin_tokens(OL, T, seed=300 + T, alpha=alpha)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, T)
+    y = torch.empty((T, W.d_model), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, from_bits(x).cuda(), T, y, idx, w, ws)
+    torch.cuda.synchronize()
+    assert smoe.smoe_read_device_status(ws) == 0
+    ref = orc.moe_tokens(OL, x)
+    assert np.array_equal(host(idx), ref["idx"])
+    np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
+    assert max_row_rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+
+
 def test_q2_unsupported_calls_return_status(smoe):
-    """Q2 prefill is not built, nor Q2 decode outside the one-kernel plan
-    (d_model 128): both return SMOE_ERR_UNSUPPORTED and enqueue nothing; a
-    stack mixing Q2 and Q4 layers is an invalid argument."""
+    """Q2 outside its kernels' plans -- prefill with d_model 192 (not a
+    multiple of the 128-row tensor-core tile), decode with d_model 128 --
+    returns SMOE_ERR_UNSUPPORTED and enqueues nothing; a stack mixing Q2 and
+    Q4 layers is an invalid argument."""
     W, _ = q2_layer("f512")
     L = smoe.Layer(W)
-    ws = smoe.workspace(L, 64)
     x = synth.hidden(4, 512, seed=1, device="cuda")
+    Wo = synth.layer_weights(192, 24, 320, 3, seed=5, device="cuda", rms_norm=True, code_bits=2)
+    Lo = smoe.Layer(Wo)
+    xo = synth.hidden(4, 192, seed=1, device="cuda")
     with pytest.raises(smoe.SmoeError) as e:
-        smoe.smoe_moe_prefill_chunk(L, x, 4, torch.empty_like(x), ws=ws)
+        smoe.smoe_moe_prefill_chunk(Lo, xo, 4, torch.empty_like(xo), ws=smoe.workspace(Lo, 4))
     assert e.value.status == smoe.SMOE_ERR_UNSUPPORTED
     Wt = synth.layer_weights(128, 16, 128, 4, seed=2, device="cuda", rms_norm=True, code_bits=2)
     Lt = smoe.Layer(Wt)
