@@ -565,6 +565,12 @@ def our_arm(args):
             log("[bench] timing the oracle on the host cores")
             line["cpu_baseline"] = cpu_baseline_oracle(stack, states, args.cpu_tokens,
                                                        args.cpu_layers)
+    pre30 = None
+    if rank == 0 and ws_ == 1:
+        # prefill on the 30B shape, SMOE-Q4 here and SMOE-Q2 below (same prompts, same router draw)
+        alpha30, u30 = calibrate_alpha(smoe, synth, stack.L[0], dev)
+        pre30 = {"alpha": round(alpha30, 4), "layer0_union_64tok": u30,
+                 "q4": time_prefill(stack, smoe, synth, dev, [512, 4096], alpha30)}
     del stack
     torch.cuda.empty_cache()
 
@@ -579,6 +585,11 @@ def our_arm(args):
                              "us_per_layer": round(msq2 * 1e3 / L30, 2),
                              "effective_gbs": round(bq2 / (msq2 / 1e3) / 1e9, 1),
                              "bytes_per_token": bq2}
+        alpha_q2, u_q2 = calibrate_alpha(smoe, synth, q2.L[0], dev)
+        pre30["q2"] = time_prefill(q2, smoe, synth, dev, [512, 4096], alpha_q2)
+        pre30["q2_alpha"], pre30["q2_layer0_union_64tok"] = round(alpha_q2, 4), u_q2
+        line["prefill_30b"] = dict(workload="30B-shaped 48-layer layer-major prefill, chunks of 64, "
+                                            "SMOE-Q4 and SMOE-Q2 stacks", **pre30)
         del q2
         torch.cuda.empty_cache()
         log("[bench] dense matvec and quantiser")
