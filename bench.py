@@ -409,7 +409,7 @@ def time_dense(smoe, synth, dev, hbm_peak):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     nb = W.numel() * 2 + codes.numel() + scale.numel() * 4
-    quant = {"kernel": "k_quantize_q4", "workload": f"30B layer gate tensor {E}x{F}x{D} bf16 -> SMOE-Q4",
+    quant = {"kernel": "k_quantize<4>", "workload": f"30B layer gate tensor {E}x{F}x{D} bf16 -> SMOE-Q4",
              "ms": round(ms, 4), "gbs": round(nb / (ms / 1e3) / 1e9, 1),
              "frac": round(nb / (ms / 1e3) / 1e9 / hbm_peak, 4), "bytes": nb}
     del W, codes, scale, bias
