@@ -412,7 +412,20 @@ def time_dense(smoe, synth, dev, hbm_peak):
     quant = {"kernel": "k_quantize<4>", "workload": f"30B layer gate tensor {E}x{F}x{D} bf16 -> SMOE-Q4",
              "ms": round(ms, 4), "gbs": round(nb / (ms / 1e3) / 1e9, 1),
              "frac": round(nb / (ms / 1e3) / 1e9 / hbm_peak, 4), "bytes": nb}
-    del W, codes, scale, bias
+    codes2 = torch.empty((E, F, D // 4), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        smoe.smoe_quantize_q2(W, codes2, scale, bias)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        smoe.smoe_quantize_q2(W, codes2, scale, bias)
+    e1.record()
+    torch.cuda.synchronize()
+    ms2 = e0.elapsed_time(e1) / reps
+    nb2 = W.numel() * 2 + codes2.numel() + scale.numel() * 4
+    quant["q2"] = {"kernel": "k_quantize<2>", "ms": round(ms2, 4), "gbs": round(nb2 / (ms2 / 1e3) / 1e9, 1),
+                   "frac": round(nb2 / (ms2 / 1e3) / 1e9 / hbm_peak, 4), "bytes": nb2}
+    del W, codes, codes2, scale, bias
     torch.cuda.empty_cache()
     return dense, quant
 

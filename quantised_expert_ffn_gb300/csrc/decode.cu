@@ -1,5 +1,7 @@
 // decode.cu -- batch-1 SMOE-Q4 expert FFN: gate+up fused, then down with the
-// weighted sum into the residual.
+// weighted sum into the residual.  The three-kernel path for shapes outside
+// the one-kernel plan of decode_fused.cu (SMOE-Q4 only: SMOE-Q2 layers run on
+// that plan or are refused).
 //
 // "Optimizations" page, "Coalesced GPU Kernels -- Expert FFN and Dense
 // Matvec": lanes of one 32-wide group share an output row and read

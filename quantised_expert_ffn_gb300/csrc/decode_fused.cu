@@ -10,23 +10,29 @@
 //
 // At batch 1 a layer is a chain of three dependent steps (route -> gate/up ->
 // down) over ~22 MB (30B shape) to ~86 MB (235B shape) of weights, a few
-// microseconds of HBM time, so latency is the cost.  One CTA per SM runs the
-// whole layer with two grid-wide barriers (one 64-bit arrival counter that
-// only grows, on its own cache line; wall-clock-bounded polling):
+// microseconds of HBM time, so latency is the cost.  One CTA per SM (14
+// compute warps + 1 producer warp) runs the whole layer; grid-wide barriers
+// use one 64-bit arrival counter that only grows, on its own cache line, with
+// wall-clock-bounded polling:
 //   phase 0  CTA c < E loads router row c before it waits for the previous
-//            kernel (programmatic dependent launch), normalises x (fp32, the
-//            stand-alone router's arithmetic) and writes logit c;  -- barrier
-//   phase 1  every CTA ranks the E logits itself; a producer warp streams this
-//            CTA's gate/up rows and then its down rows with 1-D bulk async
-//            copies (cp.async.bulk, the TMA engine) into a 4-slot shared-
-//            memory ring; 16 compute warps turn gate/up rows into h = SiLU(g)*u
-//            and store it, fp32, straight into the layout the down phase
-//            reads;                                                -- barrier
-//   phase 2  one bulk copy brings all of h into shared memory; the down rows
-//            (mostly resident already) times h, combined in rank order with
-//            the residual: y = x + sum_i w_i o_i.
-// Per-row arithmetic as in decode.cu: a code q becomes the float 128+q by one
-// byte permute; per 32-code chunk s*sum((128+q)x) + (b-128s)*sum(x).
+//            kernel (programmatic dependent launch) or layer, normalises x
+//            (fp32, the stand-alone router's arithmetic) and writes logit c;
+//                                                                 -- barrier
+//   phase 1  every CTA ranks the E logits itself and hands the ranked ids to
+//            the producer warp, which streams this CTA's gate/up rows and then
+//            its down rows with 1-D bulk async copies (cp.async.bulk, the TMA
+//            engine) into a 3-slot shared-memory ring; the compute warps turn
+//            gate/up rows into h = SiLU(g)*u and store it, fp32, straight into
+//            the layout the down phase reads;                     -- barrier
+//   phase 2  one bulk copy brings all of h into shared memory and each thread
+//            keeps its 32 values of h in registers; the down rows (mostly
+//            resident already) times h, combined in rank order with the
+//            residual: y = x + sum_i w_i o_i.
+// The stack variant runs every layer of a token in one launch, a grid barrier
+// between layers.  kQ2 selects SMOE-Q2 codes (a 32-code chunk is 8 bytes
+// instead of 16); everything else is shared.
+// Per-row arithmetic: a code q becomes the float 128+q by one byte permute;
+// per 32-code chunk s*sum((128+q)x) + (b-128s)*sum(x).
 //
 // Every wait (mbarrier or grid barrier) is bounded in wall time; on timeout
 // the kernel records SMOE_ERR_TIMEOUT in the status word and runs to the end.

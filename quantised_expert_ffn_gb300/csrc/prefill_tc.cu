@@ -38,7 +38,8 @@
 // (e0,e4),(e1,e5),(e2,e6),(e3,e7) -- the order the fp16 magic-number unpack
 // produces them in.  The activation side (x for gate/up, h for down) is stored
 // with the same permutation of each 8-element block, so the contraction is
-// unchanged.
+// unchanged.  kQ2 selects SMOE-Q2 codes (16 per 32-bit word); their dequant
+// emits the same element order, so nothing else changes.
 #include <cuda.h>
 
 #include <algorithm>

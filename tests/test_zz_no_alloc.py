@@ -56,3 +56,16 @@ def test_noalloc_rejects_layers_beyond_its_scratch(smoe):
     with pytest.raises(smoe.SmoeError) as e:
         smoe.smoe_moe_decode_noalloc(L, x, torch.empty_like(x))
     assert e.value.status == smoe.SMOE_ERR_WORKSPACE
+
+
+def test_noalloc_q2_layer(smoe):
+    """An SMOE-Q2 layer through the fixed scratch equals the workspace call."""
+    W = synth.layer_weights(2048, 128, 768, 8, seed=4343, device="cuda", rms_norm=True, code_bits=2)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 1)
+    x = synth.hidden(1, 2048, seed=98, device="cuda")[0]
+    y_ref, y = torch.empty_like(x), torch.empty_like(x)
+    smoe.smoe_moe_decode(L, x, y_ref, ws=ws)
+    smoe.smoe_moe_decode_noalloc(L, x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
