@@ -251,7 +251,11 @@ int smoe_moe_decode_noalloc(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf
  * memory, read (w, x) or written (y) once.  rows >= 1; cols a multiple of 8
  * and at most 8192 (else SMOE_ERR_UNSUPPORTED).  No workspace; nothing is
  * allocated.  The sums run in fp32 (each lane's chunks in two partial sums,
- * a warp tree, then the 8 warp sums in order). */
+ * a warp tree, then the 8 warp sums in order).  w is taken as constant
+ * weights: the kernel requests its first rows before it waits for the
+ * previous kernel in the stream (programmatic dependent launch), so w must
+ * not be written by a kernel that may still run when the call starts; x may
+ * come from the previous kernel. */
 int smoe_dense_matvec(const smoe_bf16 *w, const smoe_bf16 *x, int rows, int cols, float *y,
                       smoe_stream stream);
 

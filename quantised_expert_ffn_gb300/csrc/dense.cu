@@ -19,9 +19,11 @@
 //   * per row: packed fp32 FMAs (two partial sums per lane), a warp tree, then
 //     the 8 warp sums in warp order from shared memory (double-buffered, one
 //     barrier per row block);
-//   * launched as a programmatic dependent launch, so that back-to-back calls
-//     (decode's projections) overlap one launch's start with the previous
-//     kernel's tail.
+//   * launched as a programmatic dependent launch: the first step's weights
+//     are requested before the kernel waits for the previous one in the
+//     stream (only x can depend on it), so back-to-back calls (decode's
+//     projections) overlap a launch and its first DRAM latency with the
+//     previous kernel's tail.
 //
 // Quantiser: the offline step that turns bf16 expert weights into the Q4
 // layout ("System Overview", "The Four-Component Architecture": the Sculptor's
@@ -61,8 +63,27 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int NC = cols >> 3;                                 // 16-byte chunks per row
     const int c0 = NC * warp / kMvWarps, c1 = NC * (warp + 1) / kMvWarps;
-    // launched as a programmatic dependent: nothing is read before the
-    // previous kernel in the stream has completed
+    // CTA b owns rows [rows*b/G, rows*(b+1)/G), taken RB at a time
+    const int r_beg = (int)((long long)rows * blockIdx.x / gridDim.x);
+    const int r_end = (int)((long long)rows * (blockIdx.x + 1) / gridDim.x);
+    uint4 wv[RB][CPL];
+    auto load_step = [&](int r0) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const int c = c0 + lane + 32 * j;
+                wv[r][j] = (c < c1 && r0 + r < r_end)
+                               ? ld_stream16(w + (size_t)(r0 + r) * cols + 8 * (size_t)c)
+                               : make_uint4(0, 0, 0, 0);
+            }
+    };
+    // Launched as a programmatic dependent: the weights (constant inputs) of
+    // the first step are requested while the previous kernel in the stream may
+    // still run; x, which that kernel may produce, and y only after it is done.
+    // (Not with x in shared memory: there the early loads would stay live
+    // across the staging of x and spill.)
+    if (!XS) load_step(r_beg);
     pdl_wait();
     pdl_launch_dependents();
     float2 xr[XS ? 1 : CPL][4];
@@ -81,21 +102,9 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm)
             xr[j][3] = bf16x2_f32(v.w);
         }
     }
-    // CTA b owns rows [rows*b/G, rows*(b+1)/G), taken RB at a time
-    const int r_beg = (int)((long long)rows * blockIdx.x / gridDim.x);
-    const int r_end = (int)((long long)rows * (blockIdx.x + 1) / gridDim.x);
     int buf = 0;
     for (int r0 = r_beg; r0 < r_end; r0 += RB) {
-        uint4 wv[RB][CPL];
-#pragma unroll
-        for (int r = 0; r < RB; ++r)
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const int c = c0 + lane + 32 * j;
-                wv[r][j] = (c < c1 && r0 + r < r_end)
-                               ? ld_stream16(w + (size_t)(r0 + r) * cols + 8 * (size_t)c)
-                               : make_uint4(0, 0, 0, 0);
-            }
+        if (XS || r0 != r_beg) load_step(r0);
         float acc[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
