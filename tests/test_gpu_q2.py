@@ -222,3 +222,65 @@ def test_quantise_then_decode_q2(smoe, orc):
         ref = orc.moe_token(OL, x[t])
         assert np.array_equal(host(idx), ref["idx"])
         assert rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+
+
+def _margin_ok(orc, OL, r, Wabs, K):
+    xn = orc.rmsnorm(OL, r)
+    lg = orc.router_logits(OL, xn)
+    tau = 64 * 2.0 ** -24 * float((Wabs @ np.abs(bf16_f64(xn))).max())
+    top = np.sort(lg)[::-1][:K + 1]
+    return bool(np.all(top[:-1] - top[1:] >= 10 * tau))
+
+
+def test_q2_skewed_prefill_chunk(smoe, orc):
+    """SMOE-Q2 prefill of a Zipf(1.2)-biased 64-token chunk whose largest bucket
+    holds 30-60 tokens (N up to 64 on the tensor cores) against the oracle."""
+    W, OL = q2_layer("30b", seed=23)
+    D, E, K = W.d_model, W.n_experts, W.top_k
+    Wabs = np.abs(bf16_f64(OL.router_w))
+    L = smoe.Layer(W)
+    chosen = None
+    for scale in (1.0, 1.5, 2.0, 3.0, 4.0, 6.0):
+        cand = bits(synth.zipf_bias_hidden(256, W.router_w.float(), 1.2, scale, seed=33))
+        keep = [r for r in cand if _margin_ok(orc, OL, r, Wabs, K)][:64]
+        if len(keep) < 64:
+            continue
+        x = np.stack(keep)
+        idx_ref = np.stack([orc.topk(orc.router_logits(OL, orc.rmsnorm(OL, r)), K) for r in x])
+        sizes = np.bincount(idx_ref.ravel(), minlength=E)
+        if 30 <= sizes.max() <= 60:
+            chosen = (x, sizes)
+            break
+    assert chosen is not None, "no bias scale gave a 30-60 token bucket"
+    x, sizes = chosen
+    ws = smoe.workspace(L, 64)
+    y = torch.empty((64, D), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((64, K), dtype=torch.int32, device="cuda")
+    smoe.smoe_moe_prefill_chunk(L, from_bits(x).cuda(), 64, y, idx, None, ws)
+    torch.cuda.synchronize()
+    assert smoe.smoe_read_device_status(ws) == 0
+    ref = orc.moe_tokens(OL, x)
+    assert np.array_equal(host(idx), ref["idx"])
+    assert max_row_rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+
+
+def test_q2_ffn_repeated_ids(smoe, orc):
+    """SMOE-Q2 FFN with the same expert in several slots."""
+    W, OL = q2_layer("f1536", seed=29)
+    D, E, K = W.d_model, W.n_experts, W.top_k
+    rng = np.random.default_rng(6)
+    x = bits(synth.hidden(1, D, seed=34))[0]
+    idx = rng.choice(E, K, replace=True).astype(np.int32)
+    idx[1] = idx[0]
+    idx[3] = idx[0]
+    w = rng.uniform(0.05, 1.0, K).astype(np.float32)
+    L = smoe.Layer(W)
+    ws = smoe.workspace(L, 1)
+    y = torch.empty(D, dtype=torch.bfloat16, device="cuda")
+    eo = torch.empty((K, D), dtype=torch.float32, device="cuda")
+    smoe.smoe_moe_ffn_decode(L, from_bits(x).cuda(), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), y, eo, ws)
+    torch.cuda.synchronize()
+    xn = orc.rmsnorm(OL, x)
+    o = np.stack([orc.expert_ffn(OL, int(e), xn)[0] for e in idx])
+    assert max_row_rel_l2(host(eo), o) <= TOL
+    assert rel_l2(bf16_f64(host(y)), bf16_f64(x) + (w.astype(np.float64)[:, None] * o).sum(0)) <= TOL
