@@ -23,7 +23,10 @@
 //            its down rows with 1-D bulk async copies (cp.async.bulk, the TMA
 //            engine) into a 3-slot shared-memory ring; the compute warps turn
 //            gate/up rows into h = SiLU(g)*u and store it, fp32, straight into
-//            the layout the down phase reads;                     -- barrier
+//            the layout the down phase reads (while the layer's first item is
+//            still in flight they run the row code once on the slot as it
+//            stands and discard the result, so that item does not run cold);
+//                                                                 -- barrier
 //   phase 2  one bulk copy brings all of h into shared memory and each thread
 //            keeps its 32 values of h in registers; the down rows (mostly
 //            resident already) times h, combined in rank order with the
