@@ -28,6 +28,7 @@
 // results land in shared memory and are combined in rank order with the
 // residual: y[d] = x[d] + sum_i w_i o_i[d] (fp32, one bf16 rounding).
 #include "common.cuh"
+#include "host_cache.h"
 #include "kernels.h"
 
 namespace smoe {
@@ -280,18 +281,22 @@ __global__ void __launch_bounds__(kThreads) k_decode_down(DecodeArgs a) {
     }
 }
 
-int cached_sm_count = 0;
-
 }  // namespace
 
+// SM count of the current device (cached per device; a failed query is not cached).
 int device_sm_count() {
-    if (cached_sm_count == 0) {
-        int dev = 0, n = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached_sm_count = n > 0 ? n : 1;
+    static std::atomic<int> cached[kMaxCachedDevices];
+    const int d = cache_slot();
+    if (d >= 0) {
+        const int c = cached[d].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
-    return cached_sm_count;
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    if (d >= 0) cached[d].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 size_t decode_gateup_smem(int D) {
@@ -305,12 +310,10 @@ size_t decode_down_smem(int D, int F, int K) {
 }
 
 cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t s, bool pdl) {
-    static bool attr_set = false;
+    static SmemLimits limits;
     const size_t smem = decode_gateup_smem(a.D);
-    if (!attr_set) {
-        cudaFuncSetAttribute(k_decode_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        attr_set = true;
-    }
+    const cudaError_t e = allow_dynamic_smem(k_decode_gateup, limits, 64 * 1024);
+    if (e != cudaSuccess) return e;
     const int P = a.K * a.F;
     int grid = device_sm_count() * 2;
     if (grid > P) grid = P;
@@ -318,12 +321,10 @@ cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t s, bool pdl) 
 }
 
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t s, bool pdl) {
-    static bool attr_set = false;
+    static SmemLimits limits;
     const size_t smem = decode_down_smem(a.D, a.F, a.K);
-    if (!attr_set) {
-        cudaFuncSetAttribute(k_decode_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr_set = true;
-    }
+    const cudaError_t e = allow_dynamic_smem(k_decode_down, limits, 200 * 1024);
+    if (e != cudaSuccess) return e;
     const int R = down_rows_per_cta(a.D);
     return launch_kernel(k_decode_down, dim3((a.D + R - 1) / R), dim3(kThreads), smem, s, pdl, a);
 }

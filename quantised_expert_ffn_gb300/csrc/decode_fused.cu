@@ -40,6 +40,7 @@
 // Every wait (mbarrier or grid barrier) is bounded in wall time; on timeout
 // the kernel records SMOE_ERR_TIMEOUT in the status word and runs to the end.
 #include "common.cuh"
+#include "host_cache.h"
 #include "kernels.h"
 
 namespace smoe {
@@ -840,14 +841,10 @@ size_t fused_h_floats(int F, int K) { return (size_t)K * ((F / 32 + 7) / 8) * 25
 
 template <bool kRoute, bool kQ2>
 static cudaError_t launch_variant(const FusedArgs &a, cudaStream_t s) {
-    static int attr = 0;                      // dynamic shared memory already allowed
+    static SmemLimits limits;
     const size_t smem = a.smem_bytes;
-    if (attr < (int)smem) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_layer<kRoute, kQ2>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = (int)smem;
-    }
+    const cudaError_t e = allow_dynamic_smem(k_decode_layer<kRoute, kQ2>, limits, (int)smem);
+    if (e != cudaSuccess) return e;
     return launch_kernel(k_decode_layer<kRoute, kQ2>, dim3(a.grid), dim3(kThreadsF), smem, s, true, a);
 }
 

@@ -45,6 +45,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "host_cache.h"
 #include "kernels.h"
 
 namespace smoe {
@@ -621,12 +622,9 @@ cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtens
     // CTAs would each want all 512 TMEM columns, and the second would wait in
     // tcgen05.alloc until the first exits.
     const size_t smem = std::max<size_t>(Smem<kPair>::kBytes + 1024, 120 * 1024);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<kPair, kQ2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemLimits limits;
+    const cudaError_t e = allow_dynamic_smem(k_prefill_tc<kPair, kQ2>, limits, (int)smem);
+    if (e != cudaSuccess) return e;
     return launch_kernel(k_prefill_tc<kPair, kQ2>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
                          b[1], b[2], b[3], p);
 }
