@@ -29,6 +29,11 @@
  * of the caller, cudaStream_t; NULL = legacy default stream), so every call
  * can be captured into a CUDA graph.
  *
+ * Devices.  Every call runs on the caller's current CUDA device, and `stream`
+ * must belong to it.  One process may use the library on several devices:
+ * its host-side caches (SM count, kernel attributes, the no-workspace decode
+ * scratch) are kept per device.
+ *
  * Types.  bf16 tensors are passed as smoe_bf16 (the raw 16-bit pattern of a
  * bfloat16).  Shapes are row-major, outermost first.
  *
@@ -50,7 +55,9 @@
  * (smoe_moe_decode, smoe_moe_ffn_decode, smoe_moe_decode_layers,
  * smoe_moe_decode_noalloc) takes Q2 layers whose shape fits the one-kernel
  * decode plan (d_model a multiple of 512 up to 4096, ffn_dim a multiple of
- * 128); other Q2 shapes and Q2 prefill return SMOE_ERR_UNSUPPORTED.
+ * 128); prefill (smoe_moe_prefill_chunk) takes Q2 layers on its tensor-core
+ * path (d_model and ffn_dim multiples of 128).  Other Q2 shapes return
+ * SMOE_ERR_UNSUPPORTED before anything is enqueued.
  *
  * Workspace.  Calls that need scratch take `ws`/`ws_bytes`: device memory of
  * at least smoe_workspace_bytes() bytes, 256-byte aligned, that the caller
