@@ -24,10 +24,14 @@
  * Conventions shared by every entry point
  *
  * Memory.  Every pointer is caller-owned DEVICE memory unless a parameter
- * says otherwise.  The library never allocates, never frees and never
- * synchronises the stream; all work is enqueued on `stream` (the CUDA stream
- * of the caller, cudaStream_t; NULL = legacy default stream), so every call
- * can be captured into a CUDA graph.
+ * says otherwise.  The library never allocates and never frees; apart from
+ * smoe_read_device_status, which synchronises `stream`, all work is enqueued
+ * on `stream` (the CUDA stream of the caller, cudaStream_t; NULL = legacy
+ * default stream).  The first call of an entry point on a device also sets
+ * its kernels' attributes there (a host-side step), so make it outside any
+ * stream capture.  This library's benchmark replays smoe_moe_decode_layers,
+ * smoe_moe_prefill_chunk and smoe_dense_matvec (and, with its per-layer
+ * option, smoe_moe_decode) from CUDA graphs captured after such a first call.
  *
  * Devices.  Every call runs on the caller's current CUDA device, and `stream`
  * must belong to it.  One process may use the library on several devices:
