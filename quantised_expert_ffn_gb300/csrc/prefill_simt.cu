@@ -154,14 +154,32 @@ __global__ void __launch_bounds__(kThreads) k_prefill_combine(PrefillArgs a) {
         wt[threadIdx.x] = a.w[t * a.K + threadIdx.x];
     }
     __syncthreads();
-    // CTA (t, blockIdx.y) covers elements [1024*by, 1024*by + 1024) of token t
-    const int dend = min(a.D, (int)(blockIdx.y + 1) * 1024);
-    for (int d = blockIdx.y * 1024 + threadIdx.x; d < dend; d += kThreads) {
-        float y = bf16_to_f32(a.x[(size_t)t * a.D + d]);
-        for (int i = 0; i < a.K; ++i)
-            if (slot[i] >= 0) y = fmaf(wt[i], __ldcg(a.obuf + (size_t)slot[i] * a.D + d), y);
-        a.y[(size_t)t * a.D + d] = f32_to_bf16(y);
-    }
+    // CTA (t, blockIdx.y) covers elements [1024*by, 1024*by + 1024) of token t,
+    // four consecutive ones per thread (D is a multiple of 64).  All K slot
+    // rows are requested before the sums, which then run in rank order.
+    const int d = (blockIdx.y * kThreads + threadIdx.x) * 4;
+    if (d >= a.D) return;
+    float4 o[kMaxTopK];
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i)
+        o[i] = (i < a.K && slot[i] >= 0)
+                   ? __ldcg(reinterpret_cast<const float4 *>(a.obuf + (size_t)slot[i] * a.D + d))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint2 xr = *reinterpret_cast<const uint2 *>(a.x + (size_t)t * a.D + d);
+    float y0 = __uint_as_float(xr.x << 16), y1 = __uint_as_float(xr.x & 0xFFFF0000u);
+    float y2 = __uint_as_float(xr.y << 16), y3 = __uint_as_float(xr.y & 0xFFFF0000u);
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i)
+        if (i < a.K && slot[i] >= 0) {
+            y0 = fmaf(wt[i], o[i].x, y0);
+            y1 = fmaf(wt[i], o[i].y, y1);
+            y2 = fmaf(wt[i], o[i].z, y2);
+            y3 = fmaf(wt[i], o[i].w, y3);
+        }
+    uint2 yr;
+    yr.x = (uint32_t)f32_to_bf16(y0) | ((uint32_t)f32_to_bf16(y1) << 16);
+    yr.y = (uint32_t)f32_to_bf16(y2) | ((uint32_t)f32_to_bf16(y3) << 16);
+    *reinterpret_cast<uint2 *>(a.y + (size_t)t * a.D + d) = yr;
 }
 
 cudaError_t launch_prefill_combine(const PrefillArgs &a, cudaStream_t s, bool pdl) {
