@@ -104,11 +104,10 @@ int cuda_status(cudaError_t e) {
 // Decode engine: 1 = fused one-kernel layer, 0 = three kernels (router, gate/up,
 // down).  SMOE_DECODE_PATH=split selects the latter (cross-check).
 int decode_path() {
-    static int v = -1;
-    if (v < 0) {
+    static const int v = [] {
         const char *e = getenv("SMOE_DECODE_PATH");
-        v = (e && strcmp(e, "split") == 0) ? 0 : 1;
-    }
+        return (e && strcmp(e, "split") == 0) ? 0 : 1;
+    }();   // read once (thread-safe static initialisation)
     return v;
 }
 
@@ -116,11 +115,10 @@ int decode_path() {
 // hand-written kernels of this library; SMOE_PREFILL_PATH=simt selects the
 // CUDA-core one (used to cross-check the two).
 int prefill_path() {
-    static int v = -1;
-    if (v < 0) {
+    static const int v = [] {
         const char *e = getenv("SMOE_PREFILL_PATH");
-        v = (e && strcmp(e, "simt") == 0) ? 0 : 1;
-    }
+        return (e && strcmp(e, "simt") == 0) ? 0 : 1;
+    }();
     return v;
 }
 
