@@ -95,8 +95,18 @@ EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_sta
             "smoe_quantize_q2")
 
 
+def _dev_ptr(t: torch.Tensor, what: str = "tensor") -> int:
+    """Address of a contiguous CUDA tensor.  A host tensor is refused here: its
+    address would reach the kernels as a device pointer."""
+    if not t.is_cuda:
+        raise ValueError(f"libsmoe takes device tensors; {what} is on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"libsmoe takes contiguous (row-major) tensors; {what} is not")
+    return t.data_ptr()
+
+
 def _p(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else ctypes.c_void_p(_dev_ptr(t))
 
 
 def _stream(stream=None):
@@ -130,13 +140,11 @@ class Layer:
         s.group_size = 64
         s.norm_topk_prob = int(bool(w.norm_topk_prob))
         s.rms_eps = float(w.rms_eps)
-        s.rms_gain = None if w.rms_gain is None else w.rms_gain.data_ptr()
+        s.rms_gain = None if w.rms_gain is None else _dev_ptr(w.rms_gain, "rms_gain")
         s.code_bits = int(getattr(w, "code_bits", 4))
         for n in ("router_w", "gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q",
                   "down_s", "down_b"):
-            t = getattr(w, n)
-            assert t.is_cuda and t.is_contiguous(), n
-            setattr(s, n, t.data_ptr())
+            setattr(s, n, _dev_ptr(getattr(w, n), n))
         self.s = s
         self.ref = ctypes.byref(s)
 

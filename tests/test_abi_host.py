@@ -175,3 +175,17 @@ def test_status_strings(lib):
     for code in range(-6, 1):
         assert lib.smoe_status_string(code).startswith("SMOE_")
     assert "unknown" in lib.smoe_status_string(7)
+
+
+def test_binding_refuses_host_tensors(lib):
+    """The Python binding hands the library device pointers only: a host tensor
+    is refused before any call (its address would reach a kernel)."""
+    import torch
+    with pytest.raises(ValueError, match="device tensors"):
+        lib.smoe_dense_matvec(torch.zeros((4, 8), dtype=torch.bfloat16),
+                              torch.zeros(8, dtype=torch.bfloat16), torch.zeros(4))
+    with pytest.raises(ValueError, match="device tensors"):
+        lib.smoe_workspace_init(torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="device tensors"):
+        lib._p(torch.zeros(1))
+    assert lib._p(None) is None
