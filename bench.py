@@ -7,11 +7,15 @@ through all 48 layers (router + top-k + fused Q4 expert FFN + weighted
 residual sum, per layer), replayed from a CUDA graph; inputs are resident in
 HBM and each token reads 1.04 GB of distinct expert weights, more than L2.
 
-The JSON line also carries: the roofline of the dominant work (the decode
-expert FFN, timed per call with CUDA events), the end-to-end rate through the
-C ABI with host buffers, clocks sampled during the timed region, the oracle's
-CPU rate, a 235B-shaped 94-layer decode (per-token and per-layer time) and a
-235B-shaped layer-major prefill (prompts of 45, 512 and 4096 tokens in
+The JSON line also carries: the roofline of the step's one kernel (the decode
+launch over 48 layers: algorithmic bytes over its CUDA-event time, ncu DRAM
+traffic from profiles/ while the kernel's sources match the capture), the
+expert FFN alone per call, the end-to-end rate through the C ABI with host
+buffers, clocks sampled during the timed region, the oracle's CPU rate, the
+SMOE-Q2 decode stack, a 30B-shaped prefill (SMOE-Q4 and SMOE-Q2), the dense
+bf16 matvec on the trunk's projection shapes and the LM head, the Q4 and Q2
+quantisers, a 235B-shaped 94-layer decode (per-token and per-layer time) and
+a 235B-shaped layer-major prefill (prompts of 45, 512 and 4096 tokens in
 chunks of 64, tokens correlated so a chunk's union holds ~60-100 experts).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
