@@ -189,3 +189,28 @@ def test_binding_refuses_host_tensors(lib):
     with pytest.raises(ValueError, match="device tensors"):
         lib._p(torch.zeros(1))
     assert lib._p(None) is None
+
+
+def test_ffn_decode_and_noalloc_reject_bad_arguments_on_host(lib):
+    so = lib._lib
+    P = ctypes.c_void_p
+    s = _layer(lib)
+    ref = ctypes.byref(s)
+    ws = ctypes.c_void_p(1 << 24)
+    n = so.smoe_workspace_bytes(ref, 1)
+    ffn = lambda x=P(4096), idx=P(64), w=P(128), y=P(8192), eo=None, wsp=ws, nb=n, layer=ref: \
+        so.smoe_moe_ffn_decode(layer, x, idx, w, y, eo, wsp, nb, None)
+    assert ffn(idx=None) == lib.SMOE_ERR_INVALID_ARG          # ids are required
+    assert ffn(w=None) == lib.SMOE_ERR_INVALID_ARG            # and their weights
+    assert ffn(y=P(8194)) == lib.SMOE_ERR_INVALID_ARG         # misaligned output
+    assert ffn(eo=P(4098)) == lib.SMOE_ERR_INVALID_ARG        # misaligned expert outputs
+    assert ffn(nb=16) == lib.SMOE_ERR_WORKSPACE
+    assert ffn(layer=None) == lib.SMOE_ERR_INVALID_ARG
+    nd = so.smoe_moe_decode_noalloc
+    assert nd(None, P(4096), P(8192), None, None, None) == lib.SMOE_ERR_INVALID_ARG
+    bad = _layer(lib, D=2000)
+    assert nd(ctypes.byref(bad), P(4096), P(8192), None, None, None) == lib.SMOE_ERR_UNSUPPORTED
+    big = _layer(lib, D=8192)
+    big.ffn_dim = 2048
+    assert so.smoe_workspace_bytes(ctypes.byref(big), 1) > lib.SMOE_DECODE_NOALLOC_MAX_BYTES
+    assert nd(ctypes.byref(big), P(4096), P(8192), None, None, None) == lib.SMOE_ERR_WORKSPACE
