@@ -29,7 +29,7 @@ def _rank(rank, world, port, out):
 
 def test_replica_rate_two_gloo_ranks():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of a multi-threaded process
         out = m.dict()
         mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
