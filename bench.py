@@ -649,7 +649,11 @@ def reference_arm(args):
     from quantised_expert_ffn_gb300 import synth
     from tests.util import oracle_layer
     oracle.build()
+    # bounded run: past 128 steps (warm-up included) fewer layers per step, never fewer
+    # tokens (the tokens are what the oracle spreads over the host cores)
     n_layers = args.cpu_layers
+    if args.steps + args.warmup > 128:
+        n_layers = max(1, n_layers * 128 // (args.steps + args.warmup))
     W = [synth.layer_weights(D30, E, F30, K, seed=SEED * 1000 + i, device="cpu", rms_norm=True)
          for i in range(n_layers)]
     OL = [oracle_layer(w) for w in W]
