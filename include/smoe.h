@@ -278,11 +278,9 @@ int smoe_dense_matvec(const smoe_bf16 *w, const smoe_bf16 *x, int rows, int cols
  *   mn, mx = least and greatest weight of the group;
  *   scale  = bf16 (nearest, ties to even) of binary32 ((mx - mn) + 0) / 15;
  *   bias   = mn + 0 (exact in bf16; -0 becomes +0);
- *   q      = the integer nearest (halves to even) to d * r, with d = w - mn
- *            rounded to binary32, r = the binary32 reciprocal of scale, the
- *            product exact; the binary32 quotient d / scale instead where
- *            scale is below 2^-126; 0 wherever scale is 0.  Every code is the
- *            nearest of the 16 levels up to 2^-20 of a half step.
+ *   q      = the code of the level nearest to w: the integer nearest to the
+ *            exact quotient (w - mn) / scale, halves to even (it lies in
+ *            [0, 15]); 0 wherever scale is 0.
  * w bf16 [rows][cols] (16-byte aligned); codes uint8 [rows][cols/2]
  * (16-byte aligned), scale and bias bf16 [rows][cols/64]; caller-owned device
  * memory.  cols a multiple of 64 (else SMOE_ERR_UNSUPPORTED), rows >= 1.

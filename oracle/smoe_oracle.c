@@ -436,21 +436,27 @@ void orc_dense_matvec(const uint16_t *w, const uint16_t *x, long rows, long cols
  * Sculptor turns a model's routed experts into the vault's "aggressively
  * quantised" blocks).  The pages give no formula; this project reads it as
  * min/max affine quantisation per group of 64 consecutive weights of a row,
- * into the Q4 storage above, in binary32 with one explicit exception:
+ * into the Q4 storage above:
  *   mn, mx = the least and the greatest weight of the group (bf16, exact)
- *   scale  = bf16 nearest-even of ((mx - mn) + 0) / 15
+ *   scale  = bf16 nearest-even of the binary32 value ((mx - mn) + 0) / 15
  *   bias   = bf16 of mn + 0  (exact; the "+ 0" turns a -0 into +0)
- *   d      = w - mn, rounded to binary32
- *   q      = 0 where scale is 0; else the integer nearest (halves to even) to
- *            d * r, r = the binary32 reciprocal of scale (nearest), the
- *            product taken exactly (rounded once, to the integer); where scale
- *            is below 2^-126 (no finite binary32 reciprocal is safe), the
- *            integer nearest to the binary32 quotient d / scale.  q is clamped
- *            to [0, 15] (d * r <= 15.03, so the clamp never acts in practice).
- * A quotient by multiplication with the reciprocal is how the quantiser is
- * computed fast; rounding the exact product once keeps every code the
- * nearest level of d / scale up to 2^-20 of a half.
- * Decoding is w' = scale * q + bias, the layout's own definition. */
+ *   q      = the code of the level scale*q + bias nearest to w: the integer
+ *            nearest to the EXACT quotient (w - mn) / scale, halves to even;
+ *            0 wherever scale is 0.  (w - mn) / scale <= 15 * (1 + 2^-8), so
+ *            q never leaves [0, 15].
+ * Decoding is w' = scale * q + bias, the layout's own definition.
+ *
+ * How q is evaluated, exactly.  The integer nearest to t = d / s (d = w - mn
+ * >= 0, s > 0), halves to even, is the number of midpoints k + 1/2
+ * (k = 0 .. levels-1) that lie strictly below t, plus one for a midpoint
+ * that t hits exactly when k is odd (k + 1 is then the even neighbour).
+ * Since s > 0, "k + 1/2 < t" is "s (k + 1/2) < d".  Both sides are exact here:
+ *   - c = s (k + 1/2): 8 significant bits times at most 6, a binary64 value;
+ *   - d = w - mn is held as dh + dl, the binary64 sum and its exact rounding
+ *     error (Knuth's TwoSum; no overflow or underflow is possible for bf16
+ *     inputs in binary64).  Because rounding is monotonic, dh > c implies
+ *     d > c and dh < c implies d < c; when dh == c, d - c = dl.
+ * No reciprocal, division or other rounding enters the decision. */
 static float bf16_to_f32_orc(uint16_t h)
 {
     uint32_t u = (uint32_t)h << 16;
@@ -459,9 +465,32 @@ static float bf16_to_f32_orc(uint16_t h)
     return f;
 }
 
+/* Sign of (dh + dl) - c, exactly, for dh = RN(d), dl = d - dh, c a binary64. */
+static int cmp_exact(double dh, double dl, double c)
+{
+    if (dh != c)
+        return dh > c ? 1 : -1;
+    return dl > 0.0 ? 1 : (dl < 0.0 ? -1 : 0);
+}
+
+/* The integer nearest to (w - mn) / s, halves to even, for s > 0, w >= mn. */
+static int nearest_level(double w, double mn, double s, int levels)
+{
+    const double dh = w - mn;            /* Knuth's TwoSum: w - mn = dh + dl exactly */
+    const double bb = dh - w;
+    const double dl = (w - (dh - bb)) + (-mn - bb);
+    int q = 0;
+    for (int k = 0; k < levels; ++k) {
+        const int c = cmp_exact(dh, dl, s * ((double)k + 0.5));
+        if (c > 0 || (c == 0 && (k & 1)))
+            ++q;
+    }
+    return q;
+}
+
 /* The same reading for SMOE-Q2 (bits = 2): levels = 2^bits - 1 = 3 replaces 15
- * (scale = bf16 of ((mx - mn) + 0) / 3, codes clamped to [0, 3]), codes stored
- * as in the Q2 layout above. */
+ * (scale = bf16 of ((mx - mn) + 0) / 3, codes in [0, 3]), codes stored as in
+ * the Q2 layout above. */
 static void quantize_codes(const uint16_t *w, long rows, long cols, int bits, uint8_t *codes,
                            uint16_t *scale, uint16_t *bias)
 {
@@ -480,24 +509,13 @@ static void quantize_codes(const uint16_t *w, long rows, long cols, int bits, ui
             const float range = (mx - mn) + 0.0f;
             const float quot = range / flev;
             const uint16_t sb = orc_f64_to_bf16((double)quot);
-            const float s = bf16_to_f32_orc(sb);
+            const double s = orc_bf16_to_f64(sb);
             scale[r * ng + g] = sb;
             bias[r * ng + g] = orc_f64_to_bf16((double)(mn + 0.0f));
             uint8_t *cq = codes + r * (cols / per_byte) + g * (G / per_byte);
             memset(cq, 0, (size_t)(G / per_byte));
             for (long i = 0; i < G; ++i) {
-                int q = 0;
-                if (s != 0.0f) {
-                    const float d = bf16_to_f32_orc(p[i]) - mn;
-                    double t;
-                    if (s >= 0x1p-126f) {
-                        const float r = 1.0f / s;
-                        t = rint((double)d * (double)r);   /* 24 x 24 bits: exact in binary64 */
-                    } else {
-                        t = rint((double)(d / s));
-                    }
-                    q = t < 0.0 ? 0 : (t > (double)levels ? levels : (int)t);
-                }
+                const int q = s != 0.0 ? nearest_level(orc_bf16_to_f64(p[i]), (double)mn, s, levels) : 0;
                 cq[i / per_byte] = (uint8_t)(cq[i / per_byte] | (q << (bits * (i % per_byte))));
             }
         }

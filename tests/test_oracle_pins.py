@@ -426,6 +426,111 @@ def test_quantize_round_trip_error_bound(oracle_mod):
     assert np.array_equal(q[clear], best[clear])
 
 
+def _exact_group(wbits, levels):
+    """Brute force of the quantiser's reading on one group of 64 bf16 weights,
+    with exact rationals: scale = bf16 of the binary32 ((mx - mn) + 0) / levels
+    (numpy binary32 arithmetic, torch's bf16 rounding), bias = mn, and each code
+    the level index k in 0..levels minimising |w - (mn + scale k)|, the even k
+    on a tie.  Returns (codes, scale bits, bias bits)."""
+    from fractions import Fraction
+    wf = bf16_f64(wbits).astype(np.float32)
+    mn, mx = np.float32(wf.min()), np.float32(wf.max())
+    quot = np.float32(np.float32(np.float32(mx - mn) + np.float32(0.0)) / np.float32(levels))
+    sb = int(_bf16_bits([quot])[0])
+    s = Fraction(float(bf16_f64(np.array([sb], np.uint16))[0]))
+    m = Fraction(float(mn))
+    codes = []
+    for w in wf:
+        if s == 0:
+            codes.append(0)
+            continue
+        d = Fraction(float(w)) - m
+        codes.append(min(range(levels + 1), key=lambda k: (abs(d - s * k), k % 2)))
+    return np.array(codes), sb, int(_bf16_bits([mn + np.float32(0.0)])[0])
+
+
+def _check_against_exact(oracle_mod, W, bits_=4):
+    rows, cols = W.shape
+    quant = oracle_mod.quantize_q4 if bits_ == 4 else oracle_mod.quantize_q2
+    codes, scale, bias = quant(W)
+    for r in range(rows):
+        if bits_ == 4:
+            got = _codes_of(codes[r])
+        else:
+            got = np.stack([(codes[r] >> (2 * j)) & 3 for j in range(4)], -1).reshape(-1)
+        for g in range(cols // 64):
+            c, sb, bb = _exact_group(W[r, 64 * g:64 * g + 64], (1 << bits_) - 1)
+            assert scale[r, g] == sb and bias[r, g] == bb, (r, g)
+            assert np.array_equal(got[64 * g:64 * g + 64], c), (r, g, got[64 * g:64 * g + 64], c)
+
+
+def test_quantize_matches_exact_rational_brute_force(oracle_mod):
+    """Random groups of very different magnitudes, groups with weights near
+    zero next to a large minimum, and groups built with exact ties: every
+    scale, bias and code equals the exact-rational brute force."""
+    g = torch.Generator().manual_seed(21)
+    W = torch.randn(6, 256, generator=g) * torch.exp(2 * torch.randn(6, 1, generator=g))
+    W[0, :64] *= torch.rand(64, generator=g) ** 8            # many weights near 0
+    W[1, 5] = -1.0                                           # a large minimum ...
+    W[1, 6:12] = torch.tensor([1e-9, -1e-9, 2e-7, -3e-8, 0.0, 1e-20])   # ... with tiny weights
+    Wb = bits(W.to(torch.bfloat16))
+    # a tie group: min 0, max 15 * 0.375 (scale 0.375), weights on every midpoint
+    Wb[2, 64:128] = _bf16_bits([0.0, 15 * 0.375] + [0.375 * (k % 15 + 0.5) for k in range(62)])
+    _check_against_exact(oracle_mod, Wb, 4)
+    _check_against_exact(oracle_mod, Wb, 2)
+
+
+def test_quantize_tie_with_scale_not_a_power_of_two(oracle_mod):
+    """(w - mn) / scale = 17/2 exactly with scale = 85 * 2^-16: the nearest
+    level, halves to even, is 8.  Multiplying by the rounded binary32
+    reciprocal of the scale instead gives 9, so a quantiser that divides that
+    way fails here."""
+    mn, mx, w = -155 * 2.0 ** -14, 164 * 2.0 ** -14, 205 * 2.0 ** -17
+    W = np.zeros((1, 64), dtype=np.float32)
+    W[0, :3] = [mn, mx, w]
+    W[0, 3:] = 0.0
+    codes, scale, bias = oracle_mod.quantize_q4(_bf16_bits(W))
+    s = bf16_f64(scale)[0, 0]
+    assert s == 85 * 2.0 ** -16 and bf16_f64(bias)[0, 0] == mn
+    assert (w - mn) / s == 8.5
+    assert _codes_of(codes[0])[2] == 8
+    r = np.float32(1.0) / np.float32(s)                     # the reciprocal rule disagrees
+    assert np.rint(np.float64(np.float32(w - mn)) * np.float64(r)) == 9
+    _check_against_exact(oracle_mod, _bf16_bits(W), 4)
+
+
+def test_quantize_needs_the_exact_difference(oracle_mod):
+    """mn = -0.09375, max 0.84375: scale 1/16 and -mn = 1.5 scales exactly, so
+    w = +2^-100 lies just above the midpoint (code 2) and w = -2^-100 just
+    below it (code 1).  In binary64 (and binary32) w - mn rounds onto the
+    midpoint itself; only the exact difference tells the two apart."""
+    W = np.zeros((1, 64), dtype=np.float32)
+    W[0, :4] = [-0.09375, 0.84375, 2.0 ** -100, -(2.0 ** -100)]
+    W[0, 4:] = -0.09375
+    codes, scale, bias = oracle_mod.quantize_q4(_bf16_bits(W))
+    assert bf16_f64(scale)[0, 0] == 0.0625
+    assert np.float64(2.0 ** -100) + 0.09375 == 0.09375      # the rounded difference ties
+    assert list(_codes_of(codes[0])[:4]) == [0, 15, 2, 1]
+    _check_against_exact(oracle_mod, _bf16_bits(W), 4)
+
+
+def test_quantize_scale_below_binary32_normal_range(oracle_mod):
+    """A group whose scale is below 2^-126 (bf16 subnormal range): min 0,
+    max 15 * 2^-130; halves 2.5 and 3.5 scales round to 2 and 4, and random
+    weights in range match the exact brute force."""
+    s = 2.0 ** -130
+    W = np.zeros((2, 64), dtype=np.float32)
+    W[0, :6] = [0.0, 15 * s, 2.5 * s, 3.5 * s, 7 * s, 14.5 * s]
+    g = np.random.default_rng(3)
+    W[1] = (g.integers(0, 61, 64) * 2.0 ** -135).astype(np.float32)
+    Wb = _bf16_bits(W)
+    codes, scale, bias = oracle_mod.quantize_q4(Wb)
+    assert bf16_f64(scale)[0, 0] == s
+    assert list(_codes_of(codes[0])[:6]) == [0, 15, 2, 4, 7, 14]
+    _check_against_exact(oracle_mod, Wb, 4)
+    _check_against_exact(oracle_mod, Wb, 2)
+
+
 # ---------------------------------------------------------------- SMOE-Q2 layout
 
 def _set_code2(q, row, col, code):
