@@ -29,12 +29,15 @@
 // layout ("System Overview", "The Four-Component Architecture": the Sculptor's
 // "aggressively quantised" vault blocks).  Per group of 64 consecutive weights
 // of a row: mn, mx = least and greatest weight; scale = bf16 nearest-even of
-// ((mx - mn) + 0) / 15; bias = mn + 0; q = the integer nearest (halves to
-// even) to RN(w - mn) * RN(1 / scale), the product exact (0 where scale is 0).
-// Reading 2 bytes and writing 0.5625 per weight, it is HBM-bound once the
-// per-weight work is a few instructions: one lane per group, min/max on bf16
-// pairs, one packed subtract and one packed fused multiply-add per two
-// weights, one shift-add per code.
+// ((mx - mn) + 0) / 15; bias = mn + 0; q = the integer nearest to the exact
+// quotient (w - mn) / scale, halves to even (0 where scale is 0).  Reading 2
+// bytes and writing 0.5625 per weight, it is HBM-bound once the per-weight
+// work is a few instructions: one lane per group, min/max on bf16 pairs, and
+// per two weights a few packed fp32 operations that round RN(w - mn) *
+// RN(1 / scale) to a candidate code and measure how far the product sits from
+// it.  Only a weight within 2^-17 of a midpoint between two levels (where the
+// candidate could differ from the exact answer) takes a branch that decides
+// its code exactly.
 #include "common.cuh"
 #include "dense.h"
 #include "kernels.h"
@@ -198,16 +201,84 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return *reinterpret_cast<float2 *>(&rd);
 }
 
-// The codes (kBits = 4: SMOE-Q4, 2: SMOE-Q2) of one group of 64 weights (32
-// bf16 pairs in u), its scale and bias.  Code q = the integer nearest (halves
-// to even) to d * r, d = RN(w - mn), r = RN(1 / scale), the product exact: one
-// fused multiply-add d * r + 2^23 rounds it once, onto the integers, leaving
-// 0x4B000000 + q as its bits.  The n = 32 / kBits such words e_k of a code
-// word combine into sum_k q_k 2^(kBits k) as (sum_k e_k 2^(kBits k)) minus
-// 0x4B000000 * sum_k 2^(kBits k) (mod 2^32), one shift-add each.
+// Sign of (dh + dl) - c, exactly, where dh = RN(d), dl = d - dh and c is a
+// binary32 value: rounding is monotonic, so dh > c gives d > c, dh < c gives
+// d < c, and dh == c leaves d - c = dl.
+__device__ __forceinline__ int cmp_exact(float dh, float dl, float c) {
+    if (dh != c) return dh > c ? 1 : -1;
+    return dl > 0.f ? 1 : (dl < 0.f ? -1 : 0);
+}
+
+// Code bits (0x4B000000 + q) of one weight decided exactly: q is the integer
+// nearest to (wk - mnk) / sk, halves to even, given a candidate q0 (the bits
+// `cbits`) known to be within one of it.  wk - mnk is held as the binary32 sum
+// and its exact error (Knuth's TwoSum) and compared with the two midpoints
+// sk (q0 -+ 1/2), which are exact in binary32 (8 significant bits times at
+// most 6).
+__device__ __forceinline__ uint32_t exact_cbits(float wk, float mnk, float sk, uint32_t cbits) {
+    const float dh = __fsub_rn(wk, mnk);
+    const float bb = __fsub_rn(dh, wk);
+    const float dl = __fadd_rn(__fsub_rn(wk, __fsub_rn(dh, bb)), __fsub_rn(-mnk, bb));
+    const int q0 = (int)(cbits - 0x4B000000u);
+    const int hi = cmp_exact(dh, dl, __fmul_rn(sk, (float)q0 + 0.5f));
+    const int lo = cmp_exact(dh, dl, __fmul_rn(sk, (float)q0 - 0.5f));
+    int q = q0;
+    if (hi > 0 || (hi == 0 && (q0 & 1))) q = q0 + 1;
+    else if (lo < 0 || (lo == 0 && (q0 & 1))) q = q0 - 1;
+    return 0x4B000000u + (uint32_t)q;
+}
+
+// The codes of a group whose scale is above 2^120 (its reciprocal would be
+// near binary32's subnormal range, so no candidate is computed): every weight
+// is compared with every midpoint s (k + 1/2), exactly as in exact_cbits.
+// Such a group needs weights near 2^124 and never occurs in practice; it is
+// kept so that every finite input has its exact codes.  `row` is the lane's 64
+// weights as they sit in its swizzled shared-memory row.
 template <int kBits>
-__device__ __forceinline__ void q_group(const uint32_t (&u)[32], uint32_t (&code)[2 * kBits], uint16_t &sb,
-                                        uint16_t &bb) {
+__device__ __noinline__ void q_group_huge(const unsigned char *row, int lane, float mn, float s, uint32_t *out) {
+    constexpr int kLevels = (1 << kBits) - 1, kPerWord = 32 / kBits;
+#pragma unroll 1
+    for (int wd = 0; wd < 2 * kBits; ++wd) {
+        uint32_t acc = 0;
+#pragma unroll 1
+        for (int i = kPerWord - 1; i >= 0; --i) {
+            const int el = wd * kPerWord + i, c = el >> 3;
+            const float w = bf16_to_f32(*reinterpret_cast<const uint16_t *>(row + ((c ^ lane) & 7) * 16 + (el & 7) * 2));
+            const float dh = __fsub_rn(w, mn);
+            const float bb = __fsub_rn(dh, w);
+            const float dl = __fadd_rn(__fsub_rn(w, __fsub_rn(dh, bb)), __fsub_rn(-mn, bb));
+            uint32_t q = 0;
+            for (int k = 0; k < kLevels; ++k) {
+                const int t = cmp_exact(dh, dl, __fmul_rn(s, (float)k + 0.5f));
+                q += (t > 0 || (t == 0 && (k & 1))) ? 1u : 0u;
+            }
+            acc = (acc << kBits) + q;
+        }
+        out[wd] = acc;
+    }
+}
+
+// The codes (kBits = 4: SMOE-Q4, 2: SMOE-Q2) of one group of 64 weights (32
+// bf16 pairs in u), its scale and bias.  Per pair of weights, in packed fp32:
+//   d  = RN(w kk - mn kk)              (kk = 1, or 2^64 for a scale below 2^-62:
+//                                       a power of two, so every value stays exact)
+//   c  = RN(d r + 2^23)                 r = RN(1 / (s kk)): c holds 2^23 + q0,
+//                                       q0 = rint(d r), rounded once
+//   e  = RN(d r - q0)                   the distance from q0 in scale units
+//   t  = RN(e e - (1/4 - 2^-17))        t >= 0 only near a midpoint
+// d r is within 2^-19 of the exact (w - mn) / s, so a weight with |e| below
+// 1/2 - 2^-17 has q0 as its one nearest level; a pair with t >= 0 in either
+// weight (an exact tie, or a weight within 2^-17 of a midpoint) has both codes
+// re-decided exactly (exact_cbits) in a branch that real weights take for
+// about one weight in 600.  The n = 32 / kBits words e_k of a code word
+// combine into sum_k q_k 2^(kBits k) as (sum_k e_k 2^(kBits k)) minus
+// 0x4B000000 * sum_k 2^(kBits k) (mod 2^32), one shift-add each.  A group
+// whose scale is above 2^120 is coded by q_group_huge, which writes the codes
+// itself (returns true).
+template <int kBits>
+__device__ __forceinline__ bool q_group(const uint32_t (&u)[32], const unsigned char *row, int lane,
+                                        uint32_t (&code)[2 * kBits], uint16_t &sb, uint16_t &bb,
+                                        uint32_t *out) {
     constexpr int kWords = 2 * kBits, kPairs = 16 / kBits;  // code words; bf16 pairs per code word
     constexpr uint32_t kPackBias = kBits == 4 ? 0xFB000000u : 0xE7000000u;   // 0x4B000000 * 0x11111111 / 0x55555555
     constexpr float kLevels = (float)((1 << kBits) - 1);
@@ -225,38 +296,42 @@ __device__ __forceinline__ void q_group(const uint32_t (&u)[32], uint32_t (&code
     if (s == 0.0f) {
 #pragma unroll
         for (int k = 0; k < kWords; ++k) code[k] = 0u;
-        return;
+        return false;
     }
-    if (s >= 0x1p-126f) {
-        const float r = __frcp_rn(s);
-        const float2 mn_2 = make_float2(mn, mn), r_2 = make_float2(r, r);
-        const float2 m23 = make_float2(8388608.0f, 8388608.0f);
-#pragma unroll
-        for (int k = 0; k < kWords; ++k) {
-            uint32_t acc = 0;
-#pragma unroll
-            for (int j = kPairs - 1; j >= 0; --j) {         // elements 2j+1, 2j of the word, highest first
-                const uint32_t p = u[kPairs * k + j];
-                const float2 d = fsub2(make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)), mn_2);
-                const float2 c = ffma2(d, r_2, m23);
-                acc = (acc << kBits) + __float_as_uint(c.y);
-                acc = (acc << kBits) + __float_as_uint(c.x);
-            }
-            code[k] = acc - kPackBias;
-        }
-    } else {                                                 // scale below binary32's normal range
-#pragma unroll
-        for (int k = 0; k < kWords; ++k) {
-            uint32_t acc = 0;
-#pragma unroll
-            for (int e = 2 * kPairs - 1; e >= 0; --e) {
-                const uint32_t p = u[kPairs * k + (e >> 1)];
-                const float w = __uint_as_float((e & 1) ? (p & 0xFFFF0000u) : (p << 16));
-                acc = (acc << kBits) + (uint32_t)rintf(__fdiv_rn(__fsub_rn(w, mn), s));
-            }
-            code[k] = acc;
-        }
+    if (s > 0x1p120f) {
+        if (out) q_group_huge<kBits>(row, lane, mn, s, out);
+        return true;
     }
+    // Every weight of a group with a scale below 2^-62 is below 2^-49 in
+    // magnitude, so scaling by 2^64 is exact and overflows nothing.
+    const float kk = s < 0x1p-62f ? 0x1p64f : 1.0f;
+    const float sk = __fmul_rn(s, kk), mnk = __fmul_rn(mn, kk);
+    const float r = __frcp_rn(sk);
+    const float2 k2 = make_float2(kk, kk), nmn2 = make_float2(-mnk, -mnk), r2 = make_float2(r, r);
+    const float2 m23 = make_float2(8388608.0f, 8388608.0f);
+    const float2 ntie = make_float2(-(0.25f - 0x1p-17f), -(0.25f - 0x1p-17f));
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int j = kPairs - 1; j >= 0; --j) {             // elements 2j+1, 2j of the word, highest first
+            const uint32_t p = u[kPairs * k + j];
+            const float2 w = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+            const float2 d = ffma2(w, k2, nmn2);
+            const float2 c = ffma2(d, r2, m23);
+            const float2 e = ffma2(d, r2, fsub2(m23, c));    // m23 - c = -q0 exactly
+            const float2 t = ffma2(e, e, ntie);
+            uint32_t cx = __float_as_uint(c.x), cy = __float_as_uint(c.y);
+            if (__builtin_expect((int)(__float_as_uint(t.x) & __float_as_uint(t.y)) >= 0, 0)) {
+                cx = exact_cbits(__fmul_rn(w.x, kk), mnk, sk, cx);
+                cy = exact_cbits(__fmul_rn(w.y, kk), mnk, sk, cy);
+            }
+            acc = (acc << kBits) + cy;
+            acc = (acc << kBits) + cx;
+        }
+        code[k] = acc - kPackBias;
+    }
+    return false;
 }
 
 // Warp steps of 32 groups (4 KiB) are handed out grid-stride; lane l
@@ -303,19 +378,22 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             u[4 * c + 2] = v.z;
             u[4 * c + 3] = v.w;
         }
-        __syncwarp();                                        // stage read: free to be refilled
         const long long grp = (st0 + i * warps) * 32 + lane;
+        const bool live = grp < n_groups;
         uint32_t code[2 * kBits];
         uint16_t sb, bb;
-        q_group<kBits>(u, code, sb, bb);
-        if (grp < n_groups) {
-            uint4 *cq = reinterpret_cast<uint4 *>(codes + grp * (8 * kBits));
+        uint32_t *cq = reinterpret_cast<uint32_t *>(codes + (live ? grp : 0) * (8 * kBits));
+        const bool exact = q_group<kBits>(u, stage + lane * 128, lane, code, sb, bb, live ? cq : nullptr);
+        if (live) {
+            if (!exact) {
 #pragma unroll
-            for (int k = 0; k < kBits / 2; ++k)
-                cq[k] = make_uint4(code[4 * k], code[4 * k + 1], code[4 * k + 2], code[4 * k + 3]);
+                for (int k = 0; k < kBits / 2; ++k)
+                    reinterpret_cast<uint4 *>(cq)[k] = make_uint4(code[4 * k], code[4 * k + 1], code[4 * k + 2], code[4 * k + 3]);
+            }
             scale[grp] = sb;
             bias[grp] = bb;
         }
+        __syncwarp();                                        // stage read by every lane: free to be refilled
     }
     cp_async_wait<0>();
 }

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from quantised_expert_ffn_gb300 import synth
-from tests.util import bf16_f64, bits, host
+from tests.util import bf16_f64, bits, from_bits, host
 
 pytestmark = pytest.mark.gpu
 
@@ -131,6 +131,56 @@ def test_quantize_q4_bit_exact(smoe, orc, shape, spread):
     assert np.array_equal(host(codes).reshape(-1, cols // 2), c_ref)
     assert np.array_equal(host(scale).reshape(-1, cols // 64), s_ref)
     assert np.array_equal(host(bias).reshape(-1, cols // 64), b_ref)
+
+
+def adversarial_groups(n_groups, seed):
+    """bf16 weights [n_groups, 64] built to sit on or next to the midpoints
+    between quantisation levels: exact ties with scales that are not powers of
+    two (the 17/2 case among them), weights of magnitude 2^-100 .. 2^-1 beside
+    a minimum of -0.09375 whose scale 1/16 puts it on a midpoint, groups whose
+    scale is below 2^-126, groups of weights near 2^124 (scale above 2^120),
+    and random groups of very different magnitudes."""
+    g = np.random.default_rng(seed)
+    out = np.zeros((n_groups, 64), dtype=np.float32)
+    for i in range(n_groups):
+        kind = i % 6
+        if kind == 0:                                      # ties at mn + s (k + 1/2)
+            s = np.float32(g.integers(129, 256)) * np.float32(2.0 ** int(g.integers(-20, 0)))
+            mn = np.float32(-g.integers(1, 256) * 2.0 ** int(g.integers(-16, -4)))
+            v = mn + s * (g.integers(0, 15, 64) + 0.5)
+            v[0], v[1] = mn, mn + 15 * s
+            out[i] = v
+        elif kind == 1:                                    # tiny weights beside a midpoint minimum
+            out[i] = g.choice([-1, 1], 64) * 2.0 ** -g.integers(1, 120, 64).astype(np.float64)
+            out[i, 0], out[i, 1] = -0.09375, 0.84375
+        elif kind == 2:                                    # scale below 2^-126
+            out[i] = g.integers(0, 61, 64) * 2.0 ** -135
+        elif kind == 3:                                    # scale above 2^120
+            out[i] = g.standard_normal(64) * 2.0 ** 123
+        elif kind == 4:
+            out[i, :3] = [-155 * 2.0 ** -14, 164 * 2.0 ** -14, 205 * 2.0 ** -17]   # (w - mn) / s = 17/2
+            out[i, 3:] = g.standard_normal(61) * 0.004
+        else:
+            out[i] = g.standard_normal(64) * np.exp(3 * g.standard_normal())
+    return bits(torch.from_numpy(out).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("code_bits", [4, 2])
+def test_quantize_adversarial_groups_bit_exact(smoe, orc, code_bits):
+    """Both quantisers on groups planted on and next to the midpoints between
+    levels (where a quotient with any rounding error picks the wrong code):
+    codes, scales and biases equal the oracle's exact nearest-level codes."""
+    Wb = adversarial_groups(6 * 512, seed=code_bits).reshape(-1, 512)
+    W = from_bits(Wb).cuda()
+    rows, cols = Wb.shape
+    codes = torch.empty((rows, cols * code_bits // 8), dtype=torch.uint8, device="cuda")
+    scale = torch.empty((rows, cols // 64), dtype=torch.bfloat16, device="cuda")
+    bias = torch.empty_like(scale)
+    (smoe.smoe_quantize_q4 if code_bits == 4 else smoe.smoe_quantize_q2)(W, codes, scale, bias)
+    torch.cuda.synchronize()
+    c_ref, s_ref, b_ref = (orc.quantize_q4 if code_bits == 4 else orc.quantize_q2)(Wb)
+    assert np.array_equal(host(scale), s_ref) and np.array_equal(host(bias), b_ref)
+    assert np.array_equal(host(codes), c_ref)
 
 
 def test_quantize_q4_full_layer_tensor(smoe, orc):
