@@ -105,7 +105,8 @@ typedef enum smoe_status {
     SMOE_ERR_WORKSPACE = -3,     /* workspace missing, misaligned or too small */
     SMOE_ERR_CUDA = -4,          /* a CUDA launch or runtime call failed */
     SMOE_ERR_TIMEOUT = -5,       /* device: a bounded wait gave up */
-    SMOE_ERR_DEVICE = -6         /* device: bad data (e.g. expert id out of range) */
+    SMOE_ERR_DEVICE = -6,        /* device: bad data (e.g. expert id out of range) */
+    SMOE_ERR_RANGE = -7          /* device: a value beyond fp16's range on the tensor-core prefill */
 } smoe_status;
 
 /* One MoE layer: its shape and its device-resident parameters. */
@@ -204,10 +205,32 @@ int smoe_moe_ffn_decode(const smoe_layer *layer, const smoe_bf16 *x, const int32
  * expert's weights once and apply them to every token of its bucket (grouped
  * GEMM on the tensor cores), then y[t] = x[t] + sum_i w[t][i] o[t][i] in rank
  * order.  x, y bf16 [T][D] (y must not alias x).  Optional outputs:
- * idx_out int32 [T][k], w_out fp32 [T][k]. */
+ * idx_out int32 [T][k], w_out fp32 [T][k].
+ * Precision: the tensor cores take fp16 operands -- the normed inputs (bf16,
+ * converted exactly when |x| >= 2^-24 or 0), each weight s*q + b (one fp16
+ * rounding, exact when b = -8 s), and h = SiLU(g)*u (one fp16 rounding) --
+ * with fp32 accumulation.  A value beyond fp16's range (an input above 65504
+ * in magnitude, a group whose levels b .. b + 15 s reach past 65504, or an h
+ * that rounds to infinity) sets SMOE_ERR_RANGE in the device status word and
+ * the outputs of that call are not valid; shapes the tensor-core kernels do
+ * not take (d_model or ffn_dim not a multiple of 128) run on CUDA cores in
+ * fp32, which have no such bound. */
 int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
                            int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
                            smoe_stream stream);
+
+/* smoe_moe_prefill_chunk that also returns each token's expert outputs:
+ * expert_out fp32 [T][k][D] (16-byte aligned, caller-owned device memory)
+ * receives o[t][i] = Wdown_e (SiLU(Wgate_e xn_t) * (Wup_e xn_t)) for the
+ * expert e = idx[t][i], unweighted, in rank order -- the values the chunk's
+ * grouped GEMMs computed once per union expert and that the residual sum
+ * y[t] = x[t] + sum_i w[t][i] o[t][i] consumed.  ("Prefill Reads Each Expert
+ * Once, Not Once Per Token": the per-(token, expert) outputs of the union's
+ * single read.)  Everything else, including y, is exactly what
+ * smoe_moe_prefill_chunk computes.  expert_out must not be NULL. */
+int smoe_moe_prefill_chunk_experts(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
+                                   int32_t *idx_out_opt, float *w_out_opt, float *expert_out,
+                                   void *ws, size_t ws_bytes, smoe_stream stream);
 
 /* One decode token through n_layers routed-MoE layers, each as
  * smoe_moe_decode computes it, in ONE kernel launch ("Optimizations" page,
@@ -243,15 +266,27 @@ int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_de
  * exits.  A layer whose smoe_workspace_bytes(layer, 1) exceeds that size is
  * rejected with SMOE_ERR_WORKSPACE and nothing is enqueued.  The first call on
  * a device looks up the array's device address (once, with that device
- * current); make that first call before any stream capture.  Every call
- * zeroes the array's status word and counters (a 1 KiB cudaMemsetAsync on
- * `stream`) and allocates nothing.  All calls share the one array: calls that
- * overlap on the GPU (different streams, no ordering) race and give
- * undefined results.  x, y bf16 [D] (y may alias x); idx_out int32 [k] and
- * w_out fp32 [k] optional. */
+ * current); make that first call before any stream capture.  Arguments are
+ * checked first (as smoe_moe_decode checks them); then every call zeroes the
+ * head of the array -- its status word, route tickets and grid-barrier
+ * counter -- with a cudaMemsetAsync on `stream`, and allocates nothing.  All
+ * calls share the one array: calls that overlap on the GPU (different
+ * streams, no ordering) race and give undefined results.  x, y bf16 [D]
+ * (y may alias x); idx_out int32 [k] and w_out fp32 [k] optional.
+ * A device-side error of the call (a bounded wait that gave up, an expert
+ * id out of range) is left in the array's status word, which
+ * smoe_moe_decode_noalloc_status reads; the next call clears it. */
 #define SMOE_DECODE_NOALLOC_MAX_BYTES (512u * 1024u)
 int smoe_moe_decode_noalloc(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf16 *y,
                             int32_t *idx_out_opt, float *w_out_opt, smoe_stream stream);
+
+/* The status word that the last smoe_moe_decode_noalloc call on the current
+ * device left in the fixed scratch (0, or a negative smoe_status found on the
+ * device), copied to *status_host.  Synchronises `stream`; call it after the
+ * decode call it concerns and before the next one, which clears the word.
+ * The pages have no counterpart (see smoe_moe_decode_noalloc).  Returns
+ * SMOE_OK, SMOE_ERR_INVALID_ARG or SMOE_ERR_CUDA. */
+int smoe_moe_decode_noalloc_status(int32_t *status_host, smoe_stream stream);
 
 /* Dense bf16 matrix-vector product, y[r] = sum_c w[r][c] * x[c], fp32 sums.
  * "Optimizations" page, "Coalesced GPU Kernels -- Expert FFN and Dense
@@ -295,6 +330,24 @@ int smoe_quantize_q4(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smo
  * aligned).  Arguments and errors as smoe_quantize_q4. */
 int smoe_quantize_q2(const smoe_bf16 *w, int rows, int cols, uint8_t *codes, smoe_bf16 *scale,
                      smoe_bf16 *bias, smoe_stream stream);
+
+/* Limit, in nanoseconds of the GPU's global timer, of each grid-wide barrier
+ * wait inside the one-kernel decode (smoe_moe_decode, smoe_moe_ffn_decode,
+ * smoe_moe_decode_layers, smoe_moe_decode_noalloc when they take the
+ * one-kernel plan).  Those barriers are global-memory polls with no copy or
+ * tensor-core work outstanding on their account; a wait that reaches the
+ * limit gives up, records SMOE_ERR_TIMEOUT in the device status word and lets
+ * the kernel run to its end (results are then not valid).  Every other
+ * device wait (copies landing, tensor-core work completing) keeps its own
+ * fixed limit of 200 ms.  Process-wide; read when a call is enqueued (a CUDA
+ * graph keeps the value it was captured with).  Default 200 ms (200000000);
+ * 0 makes every barrier that has to wait at all give up (for tests of the
+ * timeout path).  The pages have no counterpart: the bound exists because a
+ * GPU kernel must never wait forever.  Always returns SMOE_OK. */
+int smoe_set_grid_wait_limit(unsigned long long limit_ns);
+
+/* The current grid-barrier wait limit in nanoseconds. */
+unsigned long long smoe_get_grid_wait_limit(void);
 
 /* Name of the last CUDA error behind an SMOE_ERR_CUDA returned on this host
  * thread ("cudaSuccess" if none), for diagnostics. */

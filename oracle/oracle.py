@@ -131,6 +131,27 @@ class OracleLayer:
         return ctypes.byref(self._s)
 
 
+def layer_from_weights(W) -> OracleLayer:
+    """An OracleLayer on the very bytes of a seeded layer (an object with the
+    attributes of the input generator's LayerWeights, tensors on any device):
+    bf16 tensors become uint16 bit patterns, codes uint8, all on the host."""
+    import torch
+
+    def host(t):
+        t = t.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+
+    return OracleLayer(
+        d_model=W.d_model, n_experts=W.n_experts, top_k=W.top_k, ffn_dim=W.ffn_dim,
+        router_w=host(W.router_w), gate_q=host(W.gate_q), gate_s=host(W.gate_s),
+        gate_b=host(W.gate_b), up_q=host(W.up_q), up_s=host(W.up_s), up_b=host(W.up_b),
+        down_q=host(W.down_q), down_s=host(W.down_s), down_b=host(W.down_b),
+        rms_gain=None if W.rms_gain is None else host(W.rms_gain), rms_eps=W.rms_eps,
+        norm_topk_prob=W.norm_topk_prob, code_bits=getattr(W, "code_bits", 4))
+
+
 def bf16_to_f64(h: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> float64 (the upper half of a binary32)."""
     h = np.asarray(h, dtype=np.uint16)
@@ -238,6 +259,22 @@ def moe_tokens(L: OracleLayer, r) -> dict:
     w = np.empty((T, K), np.float64)
     lib.orc_moe_tokens(L.ref, _ptr(r), ctypes.c_int(T), _ptr(y), _ptr(yb), _ptr(idx), _ptr(w))
     return dict(y=y, y_bf16=yb, idx=idx, w=w)
+
+
+def moe_tokens_experts(L: OracleLayer, r) -> dict:
+    """moe_tokens plus every token's unweighted expert outputs, expert_out [T, K, D]."""
+    lib = _load()
+    r = _c(r, np.uint16)
+    T, D = r.shape
+    K = L.top_k
+    y = np.empty((T, D), np.float64)
+    yb = np.empty((T, D), np.uint16)
+    idx = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float64)
+    eo = np.empty((T, K, D), np.float64)
+    lib.orc_moe_tokens_experts(L.ref, _ptr(r), ctypes.c_int(T), _ptr(y), _ptr(yb), _ptr(idx),
+                               _ptr(w), _ptr(eo))
+    return dict(y=y, y_bf16=yb, idx=idx, w=w, expert_out=eo)
 
 
 def expert_union(idx, E: int) -> dict:

@@ -341,6 +341,20 @@ void orc_moe_tokens(const orc_layer *L, const uint16_t *r, int T, double *y, uin
                       idx + (size_t)t * K, w + (size_t)t * K, NULL, NULL, NULL);
 }
 
+/* The same, also returning every token's unweighted expert outputs
+ * expert_out [T][K][D] (rank order): the per-token path above, unchanged. */
+void orc_moe_tokens_experts(const orc_layer *L, const uint16_t *r, int T, double *y,
+                            uint16_t *y_bf16, int32_t *idx, double *w, double *expert_out)
+{
+    int D = L->d_model, K = L->top_k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t)
+        orc_moe_token(L, r + (size_t)t * D, y + (size_t)t * D,
+                      y_bf16 ? y_bf16 + (size_t)t * D : NULL,
+                      idx + (size_t)t * K, w + (size_t)t * K, NULL, NULL,
+                      expert_out + (size_t)t * K * D);
+}
+
 /* ---- per-chunk expert union and token buckets ----------------------------- */
 
 /* union_ids: the distinct expert ids of idx[T][k], ascending, then -1 up to E.

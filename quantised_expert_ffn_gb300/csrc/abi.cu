@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "dense.h"
@@ -57,6 +58,22 @@ WsLayout ws_layout(const smoe_layer &L, int T) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+}  // namespace
+
+// Bytes at the head of every workspace that calls expect to find zeroed: the
+// status word, the route tickets and the grid-barrier counter (the same for
+// every layer shape and token count).
+size_t ws_head_bytes() {
+    smoe_layer L{};
+    L.d_model = kGroup;
+    L.n_experts = 1;
+    L.top_k = 1;
+    L.ffn_dim = kGroup;
+    return ws_layout(L, 1).idx;
+}
+
+namespace {
+
 int check_layer(const smoe_layer *L) {
     if (!L) return SMOE_ERR_INVALID_ARG;
     if (!L->router_w || !L->gate_q || !L->gate_s || !L->gate_b || !L->up_q || !L->up_s ||
@@ -94,6 +111,10 @@ T *at(void *ws, size_t off) {
 }
 
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Limit of each grid-barrier spin of the persistent decode kernel (ns);
+// smoe_set_grid_wait_limit changes it for calls enqueued afterwards.
+std::atomic<unsigned long long> g_grid_wait_ns{kWaitLimitNs};
 
 int cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return SMOE_OK;
@@ -139,10 +160,14 @@ RouteArgs route_args(const smoe_layer &L, const smoe_bf16 *x, void *ws, const Ws
     r.xn_out = xn;
     r.xn16_out = xn16;
     r.counters = at<int32_t>(ws, o.counters);
+    r.status = at<int32_t>(ws, o.status);
     return r;
 }
 
 }  // namespace
+
+unsigned long long grid_wait_limit_ns() { return g_grid_wait_ns.load(std::memory_order_relaxed); }
+
 }  // namespace smoe
 
 using namespace smoe;
@@ -224,8 +249,12 @@ static int launch_decode_path(const smoe_layer &L, const smoe_bf16 *x, const int
     f.expert_out = expert_out;
     f.n_layers = 1;
     f.q2 = is_q2(L) ? 1 : 0;
-    if (decode_path() == 1 && fused_plan(f, device_sm_count()))
-        return cuda_status(launch_decode_layer(f, s, idx_in == nullptr));
+    f.grid_wait_ns = grid_wait_limit_ns();
+    if (decode_path() == 1 && fused_plan(f, device_sm_count())) {
+        const cudaError_t e = launch_decode_layer(f, s, idx_in == nullptr);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
+        (void)cudaGetLastError();                           // refused, nothing enqueued: three kernels
+    }
     if (f.q2) return SMOE_ERR_UNSUPPORTED;                    // Q2 runs on the one-kernel plan only
     if (!idx_in) {
         RouteArgs r = route_args(L, x, ws, o, idx_out, w_out, nullptr, nullptr, nullptr);
@@ -337,7 +366,12 @@ int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_de
         f.act0 = act[0];
         f.act1 = act[1];
         f.q2 = is_q2(L0) ? 1 : 0;
-        if (fused_plan(f, device_sm_count())) return cuda_status(launch_decode_layer(f, s, true));
+        f.grid_wait_ns = grid_wait_limit_ns();
+        if (fused_plan(f, device_sm_count())) {
+            const cudaError_t e = launch_decode_layer(f, s, true);
+            if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
+            (void)cudaGetLastError();                       // refused, nothing enqueued: per layer
+        }
     }
     // one launch sequence per layer, activations ping-ponging in the workspace
     for (int l = 0; l < n_layers; ++l) {
@@ -351,13 +385,14 @@ int smoe_moe_decode_layers(const smoe_layer *layers, const smoe_layer *layers_de
     return SMOE_OK;
 }
 
-int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
-                           int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
-                           smoe_stream stream) {
+static int prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
+                         int32_t *idx_out_opt, float *w_out_opt, float *expert_out, void *ws,
+                         size_t ws_bytes, smoe_stream stream) {
     int st = check_layer(layer);
     if (st != SMOE_OK) return st;
     if (!x || !y || T < 1 || T > kMaxChunk || !aligned(x, 16) || !aligned(y, 16) || x == y)
         return SMOE_ERR_INVALID_ARG;
+    if (expert_out && !aligned(expert_out, 16)) return SMOE_ERR_INVALID_ARG;
     if ((st = check_ws(layer, T, ws, ws_bytes)) != SMOE_OK) return st;
     const smoe_layer &L = *layer;
     const bool tc = prefill_path() == 1 && prefill_tc_supported(L.d_model, L.ffn_dim);
@@ -396,6 +431,7 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     p.hbuf = at<__half>(ws, o.hbuf);
     p.obuf = at<float>(ws, o.obuf);
     p.y = y;
+    p.expert_out = expert_out;
     p.status = at<int32_t>(ws, o.status);
     p.num_sms = device_sm_count();
     p.q2 = is_q2(L) ? 1 : 0;
@@ -406,7 +442,27 @@ int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, s
     return cuda_status(launch_prefill_simt(p, at<smoe_bf16>(ws, o.xn), at<float>(ws, o.h32), s, true));
 }
 
+int smoe_moe_prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
+                           int32_t *idx_out_opt, float *w_out_opt, void *ws, size_t ws_bytes,
+                           smoe_stream stream) {
+    return prefill_chunk(layer, x, T, y, idx_out_opt, w_out_opt, nullptr, ws, ws_bytes, stream);
+}
+
+int smoe_moe_prefill_chunk_experts(const smoe_layer *layer, const smoe_bf16 *x, int T, smoe_bf16 *y,
+                                   int32_t *idx_out_opt, float *w_out_opt, float *expert_out,
+                                   void *ws, size_t ws_bytes, smoe_stream stream) {
+    if (!expert_out) return SMOE_ERR_INVALID_ARG;
+    return prefill_chunk(layer, x, T, y, idx_out_opt, w_out_opt, expert_out, ws, ws_bytes, stream);
+}
+
 const char *smoe_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
+
+int smoe_set_grid_wait_limit(unsigned long long limit_ns) {
+    g_grid_wait_ns.store(limit_ns, std::memory_order_relaxed);
+    return SMOE_OK;
+}
+
+unsigned long long smoe_get_grid_wait_limit(void) { return g_grid_wait_ns.load(std::memory_order_relaxed); }
 
 int smoe_dense_matvec(const smoe_bf16 *w, const smoe_bf16 *x, int rows, int cols, float *y,
                       smoe_stream stream) {
@@ -445,6 +501,7 @@ const char *smoe_status_string(int status) {
     case SMOE_ERR_CUDA: return "SMOE_ERR_CUDA: a CUDA launch or runtime call failed";
     case SMOE_ERR_TIMEOUT: return "SMOE_ERR_TIMEOUT: a bounded device wait gave up";
     case SMOE_ERR_DEVICE: return "SMOE_ERR_DEVICE: bad data found on the device";
+    case SMOE_ERR_RANGE: return "SMOE_ERR_RANGE: a value beyond fp16's range on the tensor-core prefill";
     default: return "unknown smoe status";
     }
 }

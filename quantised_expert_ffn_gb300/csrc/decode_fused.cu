@@ -127,9 +127,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 
 // Grid-wide barrier over the compute warps of all CTAs (one CTA per SM, all
-// resident).  `ctr` only grows: an arrival that returns `prev` belongs to the
-// barrier instance that ends at the next multiple of gridDim.x.
-__device__ __forceinline__ void grid_sync(unsigned long long *ctr, int32_t *status) {
+// resident: the kernel is a cooperative launch).  `ctr` only grows: an arrival
+// that returns `prev` belongs to the barrier instance that ends at the next
+// multiple of gridDim.x.  The spin gives up after `limit_ns` (a kernel
+// argument the host sets) and records SMOE_ERR_TIMEOUT; nothing else waits on
+// this spin, so giving up early only leaves the results wrong, and every CTA
+// still arrives at every barrier, so the counter stays a multiple of the grid
+// at the end of the launch.
+__device__ __forceinline__ void grid_sync(unsigned long long *ctr, int32_t *status, uint64_t limit_ns) {
     bar_compute();
     if (threadIdx.x == 0) {
         const unsigned long long G = gridDim.x;
@@ -142,7 +147,7 @@ __device__ __forceinline__ void grid_sync(unsigned long long *ctr, int32_t *stat
             while (true) {
                 asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
                 if (v >= target) break;
-                if (global_ns() - t0 > kWaitLimitNs) {
+                if (global_ns() - t0 > limit_ns) {
                     set_status(status, SMOE_ERR_TIMEOUT);
                     break;
                 }
@@ -333,11 +338,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             }
         }
         const int NG = D / kGroup;
+        const uint32_t RBg = D / 32 * kCB;
         for (int p = p0; p < p1; ++g) {
             const int i = p / F, j0 = p - i * F, n = min(a.r_gu, min(p1 - p, F - j0));
             const uint32_t s = g % kSlots;
             unsigned char *dst = ring + s * a.slot_bytes;
-            const uint32_t cb = n * (D / 32 * kCB), sb = n * NG * 2;
+            const uint32_t cb = n * RBg, sb = n * NG * 2;
             if (lane == 0) {
                 mb_wait(&empty[s], ((g / kSlots) & 1) ^ 1, a.status);
                 mb_expect(&full[s], 2 * cb + 4 * sb);
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
             mb_try(&empty[s], ((g / kSlots) & 1) ^ 1);
             const size_t row = (size_t)__shfl_sync(0xffffffffu, my_e, i) * F + j0;
             if (lane < 2) {
-                bulk_g2s(dst + lane * cb, (lane ? W.uq : W.gq) + row * (D / 32 * kCB), cb, &full[s]);
+                bulk_g2s(dst + lane * cb, (lane ? W.uq : W.gq) + row * RBg, cb, &full[s]);
             } else if (lane < 6) {
                 const uint16_t *src = lane == 2 ? W.gs : lane == 3 ? W.gb : lane == 4 ? W.us : W.ub;
                 bulk_g2s(dst + 2 * cb + (lane - 2) * sb, src + row * NG, sb, &full[s]);
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
         pdl_wait();
         pdl_launch_dependents();
     } else {
-        grid_sync(a.gctr, a.status);     // every CTA's rows of the previous layer's output are written
+        grid_sync(a.gctr, a.status, a.grid_wait_ns);     // every CTA's rows of the previous layer's output are written
     }
 
     // ids and weights given by the caller (FFN-only variant): requested now,
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 a.logits[blockIdx.x] = t;
             }
         }
-        grid_sync(a.gctr, a.status);
+        grid_sync(a.gctr, a.status, a.grid_wait_ns);
         float my = -INFINITY;
         unsigned long long mykey = 0;
         if (tid < E) {
@@ -721,7 +727,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) k_decode_layer(FusedArgs a) {
                 asm volatile("fence.proxy.async.global;" ::: "memory");   // h store -> later bulk reads
             }
             // ---- barrier: all of h written; then one bulk copy brings it in ----
-            grid_sync(a.gctr, a.status);
+            grid_sync(a.gctr, a.status, a.grid_wait_ns);
             const uint32_t hbytes = (uint32_t)(K * MC * 256 * 4);
             if (tid == 0) {
                 asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -839,13 +845,34 @@ bool fused_plan(FusedArgs &a, int num_sms) {
 // Floats of h scratch the fused kernel needs (its padded down-phase layout).
 size_t fused_h_floats(int F, int K) { return (size_t)K * ((F / 32 + 7) / 8) * 256; }
 
+// The grid barriers need every CTA resident at once, so the kernel is a
+// cooperative launch: the CTAs start only when all of them fit on the device
+// (if other kernels hold SMs, the launch waits for them instead of starting
+// part of the grid), and a device that cannot hold the grid at all (fewer
+// usable SMs, e.g. a partitioned GPU) refuses the launch with
+// cudaErrorCooperativeLaunchTooLarge before anything is enqueued.  It is also
+// a programmatic dependent launch: the prologue (router row, gain) runs while
+// the previous kernel in the stream finishes, and griddepcontrol.wait orders
+// the rest after it.
 template <bool kRoute, bool kQ2>
 static cudaError_t launch_variant(const FusedArgs &a, cudaStream_t s) {
     static SmemLimits limits;
     const size_t smem = a.smem_bytes;
     const cudaError_t e = allow_dynamic_smem(k_decode_layer<kRoute, kQ2>, limits, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_decode_layer<kRoute, kQ2>, dim3(a.grid), dim3(kThreadsF), smem, s, true, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(kThreadsF);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_decode_layer<kRoute, kQ2>, a);
 }
 
 cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route) {

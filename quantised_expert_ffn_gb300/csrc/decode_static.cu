@@ -12,34 +12,38 @@
 // weights, the gate/up activations) lives in `g_decode_scratch`, a
 // file-scope __device__ array of kStaticScratchBytes that every GPU which
 // loads the library holds until the process exits.
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = 512 * 1024;   // largest layer this entry point takes
-constexpr size_t kClearBytes = 1024;                  // status word, route tickets, grid barrier
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 // Device address of g_decode_scratch for each device, looked up once with that
 // device current.  In host code the array's name is only a host-side stand-in,
-// never a device address.
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+// never a device address.  Threads that race on a first call store the same
+// value.
+std::atomic<void *> g_scratch_ptr[kMaxDevices];
 
 int scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SMOE_ERR_CUDA;
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return SMOE_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        g_scratch_ptr[dev].store(p, std::memory_order_relaxed);
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return SMOE_OK;
 }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
 
@@ -52,12 +56,24 @@ int smoe_moe_decode_noalloc(const smoe_layer *layer, const smoe_bf16 *x, smoe_bf
     const size_t need = smoe_workspace_bytes(layer, 1);
     if (need == 0) return layer ? SMOE_ERR_UNSUPPORTED : SMOE_ERR_INVALID_ARG;
     if (need > kStaticScratchBytes) return SMOE_ERR_WORKSPACE;   // layer too large for the fixed scratch
+    // the arguments smoe_moe_decode would reject, rejected before the scratch is touched
+    if (!x || !y || !aligned16(x) || !aligned16(y)) return SMOE_ERR_INVALID_ARG;
     void *ws = nullptr;
     const int st = scratch_for_current_device(&ws);
     if (st != SMOE_OK) return st;
     // the array keeps the previous call's contents: zero the status word and counters
-    if (cudaMemsetAsync(ws, 0, kClearBytes, (cudaStream_t)stream) != cudaSuccess) return SMOE_ERR_CUDA;
+    const size_t clear = smoe::ws_head_bytes();
+    if (clear > kStaticScratchBytes) return SMOE_ERR_WORKSPACE;
+    if (cudaMemsetAsync(ws, 0, clear, (cudaStream_t)stream) != cudaSuccess) return SMOE_ERR_CUDA;
     return smoe_moe_decode(layer, x, y, idx_out_opt, w_out_opt, nullptr, ws, kStaticScratchBytes, stream);
+}
+
+int smoe_moe_decode_noalloc_status(int32_t *status_host, smoe_stream stream) {
+    if (!status_host) return SMOE_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    const int st = scratch_for_current_device(&ws);
+    if (st != SMOE_OK) return st;
+    return smoe_read_device_status(ws, status_host, stream);
 }
 
 }  // extern "C"

@@ -40,6 +40,7 @@ struct RouteArgs {
     uint16_t *xn_out;           // [T][D] bf16 or NULL
     __half *xn16_out;           // [T][D] fp16 or NULL
     int32_t *counters;          // [T], zero on entry and on exit
+    int32_t *status;            // device status word
 };
 cudaError_t launch_route_topk(const RouteArgs &a, int T, cudaStream_t s, bool pdl);
 
@@ -102,12 +103,20 @@ struct FusedArgs {
     int n_layers;               // layers run by one launch (1 unless `layers` is set)
     uint16_t *act0, *act1;      // stack variant: [D] bf16 activations between layers (ping-pong)
     int q2;                     // 1: SMOE-Q2 codes (2 bits, 8 bytes per 32 codes), 0: SMOE-Q4
+    unsigned long long grid_wait_ns;   // limit of each grid-barrier spin (smoe_set_grid_wait_limit)
     // plan (fused_plan)
     int grid, r_gu, dn_nr, dn_gran, dn_rs, rows_max, slot_bytes, ring_bytes, union_bytes, smem_bytes;
 };
 bool fused_plan(FusedArgs &a, int num_sms);
 size_t fused_h_floats(int F, int K);
+// Cooperative launch (every CTA resident before any runs); returns
+// cudaErrorCooperativeLaunchTooLarge when the device cannot hold the grid
+// (then nothing is enqueued and the caller takes the three-kernel engine).
 cudaError_t launch_decode_layer(const FusedArgs &a, cudaStream_t s, bool route);
+
+// Limit of each grid-barrier spin of the persistent decode kernel, ns
+// (process-wide; read when a call is enqueued).
+unsigned long long grid_wait_limit_ns();
 
 struct PrefillArgs {
     const uint16_t *x;          // [T][D] residual
@@ -126,6 +135,7 @@ struct PrefillArgs {
     __half *hbuf;               // [T*K][F] fp16
     float *obuf;                // [T*K][D] fp32 per-(bucket slot) expert outputs
     uint16_t *y;                // [T][D]
+    float *expert_out;          // [T][K][D] unweighted o of each (token, rank), or NULL
     int32_t *status;
     int num_sms;
     int q2;                     // 1: SMOE-Q2 codes (tensor-core path only)
@@ -139,5 +149,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_combine(const PrefillArgs &a, cudaStream_t s, bool pdl);
 
 int device_sm_count();
+
+// Bytes at the head of a workspace that must be zero before a call (status
+// word, route tickets, grid-barrier counter); the same for every layer shape.
+size_t ws_head_bytes();
 
 }  // namespace smoe

@@ -13,7 +13,8 @@
 //   warp -> row j; H[slot][j] = SiLU(gate_e . xn_t) * (up_e . xn_t) for every
 //   bucket slot (token t) of u.
 // k_prefill_down_simt: grid (D/8, E) -- warp -> row d; O[slot][d] = down_e . H[slot].
-// k_prefill_combine: y[t] = x[t] + sum_i w[t][i] O[slot(t, i)], rank order.
+// k_prefill_combine: y[t] = x[t] + sum_i w[t][i] O[slot(t, i)], rank order
+//   (and, when asked, each token's unweighted O[slot(t, i)] in rank order).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -176,6 +177,12 @@ __global__ void __launch_bounds__(kThreads) k_prefill_combine(PrefillArgs a) {
             y2 = fmaf(wt[i], o[i].z, y2);
             y3 = fmaf(wt[i], o[i].w, y3);
         }
+    if (a.expert_out) {
+#pragma unroll
+        for (int i = 0; i < kMaxTopK; ++i)
+            if (i < a.K)
+                *reinterpret_cast<float4 *>(a.expert_out + ((size_t)t * a.K + i) * a.D + d) = o[i];
+    }
     uint2 yr;
     yr.x = (uint32_t)f32_to_bf16(y0) | ((uint32_t)f32_to_bf16(y1) << 16);
     yr.y = (uint32_t)f32_to_bf16(y2) | ((uint32_t)f32_to_bf16(y3) << 16);

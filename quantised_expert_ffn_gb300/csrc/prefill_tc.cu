@@ -43,6 +43,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "host_cache.h"
@@ -223,11 +224,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 // ---- dequant ---------------------------------------------------------------
 
-// bf16 element j (runtime, 0..7) of 8 packed in a uint4, as a half2 pair.
-__device__ __forceinline__ __half2 pick_h2(const uint4 &v, int j) {
+// bf16 element j (runtime, 0..7) of 8 packed in a uint4, as a float.
+__device__ __forceinline__ float pick_f(const uint4 &v, int j) {
     const uint32_t w = (j & 4) ? ((j & 2) ? v.w : v.z) : ((j & 2) ? v.y : v.x);
-    const uint16_t b = (j & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xFFFFu);
-    return __half2half2(__float2half_rn(bf16_to_f32(b)));
+    return bf16_to_f32((j & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xFFFFu));
+}
+
+__device__ __forceinline__ __half2 f2h2(float f) { return __half2half2(__float2half_rn(f)); }
+
+// The levels b .. b + L s of a group (L = 15 for SMOE-Q4, 3 for SMOE-Q2) must
+// stay within fp16's range for the dequantised operand to be valid.
+__device__ __forceinline__ bool levels_in_fp16(float s, float b, float L) {
+    return fabsf(b) <= 65504.f && fabsf(fmaf(s, L, b)) <= 65504.f;
 }
 
 // 8 codes of one word -> 4 half2 (e_i, e_{i+4}), each s*q + b with one rounding.
@@ -437,29 +445,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int c = 0; c < NC; ++c, ++g) {
                 const int s = g % kStages, a = s;
-                __half2 s0, b0, s1, b1;
+                float s0f, b0f, s1f, b1f;
                 if (p.vec_scales) {
                     if ((c & 7) == 0 && c > 0) {
                         vs0 = ns0; vb0 = nb0; vs1 = ns1; vb1 = nb1;
                         if (c + 8 < NC) load8(c + 8, ns0, nb0, ns1, nb1);
                     }
-                    s0 = pick_h2(vs0, c & 7);
-                    b0 = pick_h2(vb0, c & 7);
-                    s1 = s0, b1 = b0;
+                    s0f = pick_f(vs0, c & 7);
+                    b0f = pick_f(vb0, c & 7);
+                    s1f = s0f, b1f = b0f;
                     if (kPair) {
-                        s1 = pick_h2(vs1, c & 7);
-                        b1 = pick_h2(vb1, c & 7);
+                        s1f = pick_f(vs1, c & 7);
+                        b1f = pick_f(vb1, c & 7);
                     }
                 } else {
                     // scales/biases of this row and group (L1-cached: 16 groups share a sector)
-                    s0 = __half2half2(__float2half_rn(bf16_to_f32(p.s0[row * NG + c])));
-                    b0 = __half2half2(__float2half_rn(bf16_to_f32(p.b0[row * NG + c])));
-                    s1 = s0, b1 = b0;
+                    s0f = bf16_to_f32(p.s0[row * NG + c]);
+                    b0f = bf16_to_f32(p.b0[row * NG + c]);
+                    s1f = s0f, b1f = b0f;
                     if (kPair) {
-                        s1 = __half2half2(__float2half_rn(bf16_to_f32(p.s1[row * NG + c])));
-                        b1 = __half2half2(__float2half_rn(bf16_to_f32(p.b1[row * NG + c])));
+                        s1f = bf16_to_f32(p.s1[row * NG + c]);
+                        b1f = bf16_to_f32(p.b1[row * NG + c]);
                     }
                 }
+                constexpr float kLv = kQ2 ? 3.f : 15.f;
+                if (!levels_in_fp16(s0f, b0f, kLv) || !levels_in_fp16(s1f, b1f, kLv))
+                    set_status(p.status, SMOE_ERR_RANGE);
+                const __half2 s0 = f2h2(s0f), b0 = f2h2(b0f), s1 = f2h2(s1f), b1 = f2h2(b1f);
                 // waits are warp-uniform: the TMEM store below is warp-collective
                 if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status))) {
                     ok = false;
@@ -533,8 +545,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int pos = perm8(orow);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (n0 + j < m)
-                            p.hout[(size_t)(off + n0 + j) * p.out_ld + pos] = __float2half_rn(silu_mul(v0[j], v1[j]));
+                        if (n0 + j < m) {
+                            const __half hv = __float2half_rn(silu_mul(v0[j], v1[j]));
+                            if (__hisinf(hv)) set_status(p.status, SMOE_ERR_RANGE);
+                            p.hout[(size_t)(off + n0 + j) * p.out_ld + pos] = hv;
+                        }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -589,16 +604,21 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once per process (threads that
+// race on the first call store the same pointer).
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_relaxed);
+    if (!f) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<EncodeTiledFn>(p);
+            fn.store(f, std::memory_order_relaxed);
+        }
     }
-    return fn;
+    return f;
 }
 
 // 2-D map over a row-major [rows][cols] array of `esize`-byte elements.

@@ -71,9 +71,12 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_topk(RouteArgs a) {
     if (blockIdx.x == 0) {
         if (a.xn_out)
             for (int d = tid; d < D; d += kRouteThreads) a.xn_out[(size_t)t * D + d] = xs[d];
-        if (a.xn16_out)
-            for (int d = tid; d < D; d += kRouteThreads)
-                a.xn16_out[(size_t)t * D + d] = __float2half_rn(bf16_to_f32(xs[d]));
+        if (a.xn16_out)   // the tensor-core prefill's fp16 copy: report values past its range
+            for (int d = tid; d < D; d += kRouteThreads) {
+                const float v = bf16_to_f32(xs[d]);
+                if (fabsf(v) > 65504.f) set_status(a.status, SMOE_ERR_RANGE);
+                a.xn16_out[(size_t)t * D + d] = __float2half_rn(v);
+            }
     }
 
     // ---- router rows: one warp per expert ----

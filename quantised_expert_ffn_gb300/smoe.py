@@ -24,6 +24,7 @@ SMOE_ERR_WORKSPACE = -3
 SMOE_ERR_CUDA = -4
 SMOE_ERR_TIMEOUT = -5
 SMOE_ERR_DEVICE = -6
+SMOE_ERR_RANGE = -7
 
 
 class SmoeError(RuntimeError):
@@ -72,13 +73,17 @@ def _load():
         "smoe_moe_decode": (I, [LP, P, P, P, P, P, P, Z, P]),
         "smoe_moe_ffn_decode": (I, [LP, P, P, P, P, P, P, Z, P]),
         "smoe_moe_prefill_chunk": (I, [LP, P, I, P, P, P, P, Z, P]),
+        "smoe_moe_prefill_chunk_experts": (I, [LP, P, I, P, P, P, P, P, Z, P]),
         "smoe_status_string": (ctypes.c_char_p, [I]),
         "smoe_moe_decode_noalloc": (I, [LP, P, P, P, P, P]),
+        "smoe_moe_decode_noalloc_status": (I, [ctypes.POINTER(ctypes.c_int32), P]),
         "smoe_moe_decode_layers": (I, [LP, P, I, P, P, P, P, P, Z, P]),
         "smoe_last_cuda_error": (ctypes.c_char_p, []),
         "smoe_dense_matvec": (I, [P, P, I, I, P, P]),
         "smoe_quantize_q4": (I, [P, I, I, P, P, P, P]),
         "smoe_quantize_q2": (I, [P, I, I, P, P, P, P]),
+        "smoe_set_grid_wait_limit": (I, [ctypes.c_ulonglong]),
+        "smoe_get_grid_wait_limit": (ctypes.c_ulonglong, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -90,9 +95,10 @@ def _load():
 _lib = _load()
 EXPORTED = ("smoe_workspace_bytes", "smoe_workspace_init", "smoe_read_device_status",
             "smoe_route_topk", "smoe_expert_union", "smoe_moe_decode", "smoe_moe_ffn_decode",
-            "smoe_moe_prefill_chunk", "smoe_status_string", "smoe_moe_decode_noalloc",
+            "smoe_moe_prefill_chunk", "smoe_moe_prefill_chunk_experts", "smoe_status_string", "smoe_moe_decode_noalloc",
+            "smoe_moe_decode_noalloc_status",
             "smoe_last_cuda_error", "smoe_moe_decode_layers", "smoe_dense_matvec", "smoe_quantize_q4",
-            "smoe_quantize_q2")
+            "smoe_quantize_q2", "smoe_set_grid_wait_limit", "smoe_get_grid_wait_limit")
 
 
 def _dev_ptr(t: torch.Tensor, what: str = "tensor") -> int:
@@ -121,6 +127,15 @@ def _check(status: int, where: str):
 
 def smoe_last_cuda_error() -> str:
     return _lib.smoe_last_cuda_error().decode()
+
+
+def smoe_set_grid_wait_limit(limit_ns: int):
+    """Limit (ns) of each grid-barrier wait of the one-kernel decode, process-wide."""
+    _check(_lib.smoe_set_grid_wait_limit(int(limit_ns)), "smoe_set_grid_wait_limit")
+
+
+def smoe_get_grid_wait_limit() -> int:
+    return int(_lib.smoe_get_grid_wait_limit())
 
 
 def smoe_status_string(status: int) -> str:
@@ -205,6 +220,15 @@ def smoe_moe_prefill_chunk(layer: Layer, x, T, y, idx_out=None, w_out=None, ws=N
            "smoe_moe_prefill_chunk")
 
 
+def smoe_moe_prefill_chunk_experts(layer: Layer, x, T, y, expert_out, idx_out=None, w_out=None,
+                                   ws=None, stream=None):
+    """smoe_moe_prefill_chunk plus the unweighted expert outputs, fp32 [T, k, D]."""
+    _check(_lib.smoe_moe_prefill_chunk_experts(layer.ref, _p(x), int(T), _p(y), _p(idx_out), _p(w_out),
+                                               _p(expert_out), _p(ws), 0 if ws is None else ws.numel(),
+                                               _stream(stream)),
+           "smoe_moe_prefill_chunk_experts")
+
+
 def smoe_dense_matvec(w, x, y, stream=None):
     """y = w @ x: w bf16 [rows, cols], x bf16 [cols], y fp32 [rows] (device tensors)."""
     rows, cols = w.shape
@@ -241,6 +265,15 @@ def smoe_moe_decode_noalloc(layer: Layer, x, y, idx_out=None, w_out=None, stream
     serving loops or plug-ins whose host owns the device memory); see include/smoe.h."""
     _check(_lib.smoe_moe_decode_noalloc(layer.ref, _p(x), _p(y), _p(idx_out), _p(w_out),
                                         _stream(stream)), "smoe_moe_decode_noalloc")
+
+
+def smoe_moe_decode_noalloc_status(stream=None) -> int:
+    """Status word the last smoe_moe_decode_noalloc call on this device left
+    (0 or a negative smoe status); synchronises the stream."""
+    out = ctypes.c_int32(0)
+    _check(_lib.smoe_moe_decode_noalloc_status(ctypes.byref(out), _stream(stream)),
+           "smoe_moe_decode_noalloc_status")
+    return int(out.value)
 
 
 class LayerTable:

@@ -214,3 +214,34 @@ def test_ffn_decode_and_noalloc_reject_bad_arguments_on_host(lib):
     big.ffn_dim = 2048
     assert so.smoe_workspace_bytes(ctypes.byref(big), 1) > lib.SMOE_DECODE_NOALLOC_MAX_BYTES
     assert nd(ctypes.byref(big), P(4096), P(8192), None, None, None) == lib.SMOE_ERR_WORKSPACE
+
+
+def test_prefill_experts_and_status_calls_reject_bad_arguments_on_host(lib):
+    so = lib._lib
+    s = _layer(lib)
+    ref = ctypes.byref(s)
+    ws = ctypes.c_void_p(1 << 24)
+    n = so.smoe_workspace_bytes(ref, 64)
+    P = ctypes.c_void_p
+    # the expert outputs are what this entry point is for: NULL or misaligned is refused
+    assert so.smoe_moe_prefill_chunk_experts(ref, P(4096), 4, P(8192), None, None, None, ws, n,
+                                             None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_moe_prefill_chunk_experts(ref, P(4096), 4, P(8192), None, None, P(1 << 20 | 4),
+                                             ws, n, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_moe_prefill_chunk_experts(ref, P(4096), 65, P(8192), None, None, P(1 << 20), ws,
+                                             n, None) == lib.SMOE_ERR_INVALID_ARG
+    assert so.smoe_moe_decode_noalloc_status(None, None) == lib.SMOE_ERR_INVALID_ARG
+
+
+def test_grid_wait_limit_round_trip(lib):
+    """The grid-barrier wait limit is plain host state: default 200 ms, set and
+    read back, restored."""
+    default = lib.smoe_get_grid_wait_limit()
+    assert default == 200_000_000
+    try:
+        for v in (0, 1, 5_000_000, 2 ** 63):
+            lib.smoe_set_grid_wait_limit(v)
+            assert lib.smoe_get_grid_wait_limit() == v
+    finally:
+        lib.smoe_set_grid_wait_limit(default)
+    assert lib.smoe_get_grid_wait_limit() == default

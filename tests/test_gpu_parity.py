@@ -2,16 +2,19 @@
 against the CPU oracle on the same seeded bytes.
 
 Bars: top-k ids, union lists and buckets bit-exact; mixing weights 1e-6
-relative (given the same logits); FFN outputs and the residual output within
-2e-3 relative L2 per token.  Inputs are drawn with routing margins (see
+relative (given the same logits); FFN outputs (fp32) within 2e-3 relative L2
+of the oracle's fp64 values; the bf16 residual output within 2e-3 relative L2
+of the oracle's y rounded once to bf16 (the rounding of a bf16 vector alone is
+about 1.6e-3 relative L2 of the unrounded value, so that is what a bf16
+output is measured against).  Inputs are drawn with routing margins (see
 tests.util.margin_tokens) so that fp32 and fp64 logits rank alike."""
 import numpy as np
 import pytest
 import torch
 
 from quantised_expert_ffn_gb300 import synth
-from tests.util import (bf16_f64, bits, from_bits, host, margin_tokens, max_row_rel_l2,
-                        oracle_layer, rel_l2)
+from tests.util import (bf16_f64, bits, from_bits, host, margin_ok, margin_tokens, max_row_rel_l2,
+                        oracle_layer, rel_l2, zipf_chunk)
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-3
@@ -211,7 +214,7 @@ def test_moe_decode(smoe, orc, name, norm, ntok):
         assert np.array_equal(host(idx), ref["idx"])
         np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
         assert max_row_rel_l2(host(eo), ref["expert_out"]) <= TOL
-        assert rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+        assert rel_l2(bf16_f64(host(y)), bf16_f64(ref["y_bf16"])) <= TOL
     assert smoe.smoe_read_device_status(ws) == 0
 
 
@@ -357,7 +360,7 @@ def test_decode_layers_against_oracle(smoe, orc):
         for i in range(2):
             assert np.array_equal(host(idx)[i], refs[i]["idx"])
             np.testing.assert_allclose(host(w)[i], refs[i]["w"], rtol=2e-5)
-        assert rel_l2(bf16_f64(host(y)), refs[1]["y"]) <= TOL
+        assert rel_l2(bf16_f64(host(y)), bf16_f64(refs[1]["y_bf16"])) <= TOL
         kept += 1
         if kept == 2:
             break
@@ -410,7 +413,7 @@ def test_moe_prefill_chunk(smoe, orc, name, norm, T, alpha):
     ref = orc.moe_tokens(OL, x)                    # = the chunk path, bit for bit (oracle pin)
     assert np.array_equal(host(idx), ref["idx"])
     np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
-    assert max_row_rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+    assert max_row_rel_l2(bf16_f64(host(y)), bf16_f64(ref["y_bf16"])) <= TOL
 
 
 def test_prefill_matches_decode_on_gpu(smoe, orc):
@@ -443,7 +446,7 @@ def test_prefill_all_tokens_one_bucket(smoe, orc):
     torch.cuda.synchronize()
     ref = orc.moe_token(OL, x1[0])
     yh = bf16_f64(host(y))
-    assert rel_l2(yh[0], ref["y"]) <= TOL
+    assert rel_l2(yh[0], bf16_f64(ref["y_bf16"])) <= TOL
     assert np.all(yh == yh[0])
 
 
@@ -464,14 +467,6 @@ def test_alternate_engines_in_subprocess(smoe):
 
 # ------------------------------------------------------------- skewed routing
 
-def _margin_ok(orc, OL, x_row, Wabs, K, factor=10.0):
-    xn = orc.rmsnorm(OL, x_row)
-    lg = orc.router_logits(OL, xn)
-    tau = 64 * 2.0 ** -24 * float((Wabs @ np.abs(bf16_f64(xn))).max())
-    top = np.sort(lg)[::-1][:K + 1]
-    return bool(np.all(top[:-1] - top[1:] >= factor * tau)), lg
-
-
 def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
     """Zipf(1.2)-biased router logits (x_t = z_t + pinv(Wr) b): a 64-token
     chunk whose largest bucket holds 30-60 tokens (at least 4x the mean bucket),
@@ -481,26 +476,9 @@ def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
     D, E, K = W.d_model, W.n_experts, W.top_k
     Wabs = np.abs(bf16_f64(OL.router_w))
     L = smoe.Layer(W)
-    chosen = None
-    for scale in (1.0, 1.5, 2.0, 3.0, 4.0, 6.0):
-        cand = bits(synth.zipf_bias_hidden(256, W.router_w.float(), 1.2, scale, seed=31))
-        keep = []
-        for r in cand:
-            ok, lg = _margin_ok(orc, OL, r, Wabs, K)
-            if ok:
-                keep.append(r)
-            if len(keep) == 64:
-                break
-        if len(keep) < 64:
-            continue
-        x = np.stack(keep)
-        idx_ref = np.stack([orc.topk(orc.router_logits(OL, orc.rmsnorm(OL, r)), K) for r in x])
-        sizes = np.bincount(idx_ref.ravel(), minlength=E)
-        if 30 <= sizes.max() <= 60:
-            chosen = (scale, x, sizes)
-            break
-    assert chosen is not None, "no bias scale gave a 30-60 token bucket"
-    scale, x, sizes = chosen
+    got = zipf_chunk(orc, OL, W.router_w, T=64, seed=31)
+    assert got is not None, "no bias scale gave a 30-60 token bucket"
+    x, sizes = got
     assert sizes.max() >= 4 * sizes.mean()                 # skewed: the largest bucket far above the mean
     ws = smoe.workspace(L, 64)
     y = torch.empty((64, D), dtype=torch.bfloat16, device="cuda")
@@ -512,7 +490,7 @@ def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
     ref = orc.moe_tokens(OL, x)
     assert np.array_equal(host(idx), ref["idx"])
     np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
-    assert max_row_rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+    assert max_row_rel_l2(bf16_f64(host(y)), bf16_f64(ref["y_bf16"])) <= TOL
 
     # decode stream with ~46% adjacent overlap (rho picked from a fixed list)
     best = None
@@ -527,7 +505,7 @@ def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
     ws1 = smoe.workspace(L, 1)
     checked = 0
     for r in stream:
-        ok, _ = _margin_ok(orc, OL, r, Wabs, K)
+        ok, _ = margin_ok(orc, OL, r, Wabs, K)
         if not ok:
             continue
         yd = torch.empty(D, dtype=torch.bfloat16, device="cuda")
@@ -536,7 +514,7 @@ def test_skewed_routing_prefill_and_overlapping_decode(smoe, orc):
         torch.cuda.synchronize()
         rr = orc.moe_token(OL, r)
         assert np.array_equal(host(ii), rr["idx"])
-        assert rel_l2(bf16_f64(host(yd)), rr["y"]) <= TOL
+        assert rel_l2(bf16_f64(host(yd)), bf16_f64(rr["y_bf16"])) <= TOL
         checked += 1
     assert checked >= 8
     assert smoe.smoe_read_device_status(ws1) == 0
@@ -561,7 +539,7 @@ def test_limits_and_degenerate_layers(smoe, orc, name):
     ref = orc.moe_token(OL, x[0])
     assert np.array_equal(host(idx), ref["idx"])
     np.testing.assert_allclose(host(w), ref["w"], rtol=2e-5)
-    assert rel_l2(bf16_f64(host(y)), ref["y"]) <= TOL
+    assert rel_l2(bf16_f64(host(y)), bf16_f64(ref["y_bf16"])) <= TOL
     if K == W.n_experts:
         assert sorted(host(idx).tolist()) == list(range(K))      # k = E: every expert, once
     if K == 1:
@@ -573,5 +551,5 @@ def test_limits_and_degenerate_layers(smoe, orc, name):
     torch.cuda.synchronize()
     refc = orc.moe_tokens(OL, x)
     assert np.array_equal(host(ic), refc["idx"])
-    assert max_row_rel_l2(bf16_f64(host(yc)), refc["y"]) <= TOL
+    assert max_row_rel_l2(bf16_f64(host(yc)), bf16_f64(refc["y_bf16"])) <= TOL
     assert smoe.smoe_read_device_status(ws) == 0

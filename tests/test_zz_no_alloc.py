@@ -27,6 +27,9 @@ def smoe():
 
 @pytest.mark.parametrize("D,E,K,F", [(2048, 128, 8, 768), (4096, 128, 8, 1536), (128, 16, 4, 128)])
 def test_noalloc_matches_workspace_decode_twice(smoe, D, E, K, F):
+    """Same kernels, same arithmetic: the output, ids and weights equal the
+    workspace call's bit for bit, on two calls in a row, and the fixed
+    scratch's status word reads 0 after each."""
     W = synth.layer_weights(D, E, F, K, seed=4242, device="cuda", rms_norm=True)
     L = smoe.Layer(W)
     assert smoe.smoe_workspace_bytes(L, 1) <= smoe.SMOE_DECODE_NOALLOC_MAX_BYTES
@@ -41,9 +44,11 @@ def test_noalloc_matches_workspace_decode_twice(smoe, D, E, K, F):
         idx = torch.full((K,), -1, dtype=torch.int32, device="cuda")
         w = torch.zeros(K, dtype=torch.float32, device="cuda")
         smoe.smoe_moe_decode_noalloc(L, xs[t], y, idx, w)
+        assert smoe.smoe_moe_decode_noalloc_status() == 0
         torch.cuda.synchronize()
         assert torch.equal(idx, idx_ref)
-        np.testing.assert_allclose(host(w), host(w_ref), rtol=1e-6)
+        assert torch.equal(w, w_ref)
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
         assert rel_l2(bf16_f64(host(y)), bf16_f64(host(y_ref))) <= TOL
     assert smoe.smoe_read_device_status(ws) == 0
 
@@ -58,6 +63,34 @@ def test_noalloc_rejects_layers_beyond_its_scratch(smoe):
     assert e.value.status == smoe.SMOE_ERR_WORKSPACE
 
 
+def test_noalloc_status_reports_a_device_error_and_the_next_call_clears_it(smoe):
+    """A device-side error of a no-workspace call is readable afterwards through
+    smoe_moe_decode_noalloc_status: with the grid-barrier wait limit at 0 the
+    call's barriers give up (SMOE_ERR_TIMEOUT); with the limit restored the
+    next call clears the word and equals the workspace call bit for bit."""
+    W = synth.layer_weights(512, 16, 128, 4, seed=5, device="cuda", rms_norm=True)
+    L = smoe.Layer(W)
+    x = synth.hidden(1, 512, seed=6, device="cuda")[0]
+    y = torch.empty_like(x)
+    default = smoe.smoe_get_grid_wait_limit()
+    try:
+        smoe.smoe_set_grid_wait_limit(0)
+        for _ in range(20):             # a call whose barriers all happen to pass at once reads 0
+            smoe.smoe_moe_decode_noalloc(L, x, y)
+            st = smoe.smoe_moe_decode_noalloc_status()
+            if st != 0:
+                break
+        assert st == smoe.SMOE_ERR_TIMEOUT
+    finally:
+        smoe.smoe_set_grid_wait_limit(default)
+    smoe.smoe_moe_decode_noalloc(L, x, y)
+    assert smoe.smoe_moe_decode_noalloc_status() == 0
+    y_ref = torch.empty_like(x)
+    smoe.smoe_moe_decode(L, x, y_ref, ws=smoe.workspace(L, 1))
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
 def test_noalloc_q2_layer(smoe):
     """An SMOE-Q2 layer through the fixed scratch equals the workspace call."""
     W = synth.layer_weights(2048, 128, 768, 8, seed=4343, device="cuda", rms_norm=True, code_bits=2)
@@ -67,5 +100,6 @@ def test_noalloc_q2_layer(smoe):
     y_ref, y = torch.empty_like(x), torch.empty_like(x)
     smoe.smoe_moe_decode(L, x, y_ref, ws=ws)
     smoe.smoe_moe_decode_noalloc(L, x, y)
+    assert smoe.smoe_moe_decode_noalloc_status() == 0
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))

@@ -3,7 +3,7 @@ oracle's numpy view (bf16 as uint16 bits)."""
 import numpy as np
 import torch
 
-from oracle.oracle import OracleLayer
+from oracle.oracle import layer_from_weights as oracle_layer  # noqa: F401  (re-exported)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -21,17 +21,6 @@ def host(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return bits(t)
     return t.detach().cpu().contiguous().numpy()
-
-
-def oracle_layer(W) -> OracleLayer:
-    """synth.LayerWeights (any device) -> OracleLayer on the same bytes."""
-    return OracleLayer(
-        d_model=W.d_model, n_experts=W.n_experts, top_k=W.top_k, ffn_dim=W.ffn_dim,
-        router_w=host(W.router_w), gate_q=host(W.gate_q), gate_s=host(W.gate_s),
-        gate_b=host(W.gate_b), up_q=host(W.up_q), up_s=host(W.up_s), up_b=host(W.up_b),
-        down_q=host(W.down_q), down_s=host(W.down_s), down_b=host(W.down_b),
-        rms_gain=None if W.rms_gain is None else host(W.rms_gain), rms_eps=W.rms_eps,
-        norm_topk_prob=W.norm_topk_prob, code_bits=getattr(W, "code_bits", 4))
 
 
 def bf16_f64(a: np.ndarray) -> np.ndarray:
@@ -78,3 +67,39 @@ def margin_tokens(OL, n, seed, *, alpha=None, tau_factor=10.0, max_tries=50):
                 if len(keep) == n:
                     return np.stack(keep)
     raise RuntimeError("could not draw enough tokens with routing margins")
+
+
+def margin_ok(orc, OL, x_row, Wabs, K, factor=10.0):
+    """Whether the oracle's top-(K+1) adjacent logit gaps of one token are all
+    at least factor * tau (see margin_tokens); also returns the logits."""
+    xn = orc.rmsnorm(OL, x_row)
+    lg = orc.router_logits(OL, xn)
+    tau = 64 * 2.0 ** -24 * float((Wabs @ np.abs(bf16_f64(xn))).max())
+    top = np.sort(lg)[::-1][:K + 1]
+    return bool(np.all(top[:-1] - top[1:] >= factor * tau)), lg
+
+
+def zipf_chunk(orc, OL, router_w, T=64, seed=31):
+    """T hidden states (bf16 bits [T, D]) whose router logits carry a Zipf(1.2)
+    bias over a seeded expert permutation, drawn with routing margins, at the
+    first bias scale whose largest bucket holds 30-60 tokens.  Returns
+    (x, bucket sizes) or None."""
+    from quantised_expert_ffn_gb300 import synth
+    K, E = OL.top_k, OL.n_experts
+    Wabs = np.abs(bf16_f64(OL.router_w))
+    for scale in (1.0, 1.5, 2.0, 3.0, 4.0, 6.0):
+        cand = bits(synth.zipf_bias_hidden(4 * T, router_w.float(), 1.2, scale, seed=seed))
+        keep = []
+        for r in cand:
+            if margin_ok(orc, OL, r, Wabs, K)[0]:
+                keep.append(r)
+            if len(keep) == T:
+                break
+        if len(keep) < T:
+            continue
+        x = np.stack(keep)
+        idx_ref = np.stack([orc.topk(orc.router_logits(OL, orc.rmsnorm(OL, r)), K) for r in x])
+        sizes = np.bincount(idx_ref.ravel(), minlength=E)
+        if 30 <= sizes.max() <= 60:
+            return x, sizes
+    return None
