@@ -168,8 +168,8 @@ cudaError_t launch_mv_rb(const uint16_t *w, const uint16_t *x, int rows, int col
 
 constexpr int kQWarps = 4;
 constexpr int kQThreads = kQWarps * 32;
-constexpr int kQCtasPerSm = 4;
-constexpr int kQStages = 3;                              // 4 KiB stages per warp
+constexpr int kQCtasPerSm = 6;                           // 24 warps per SM (registers <= 85)
+constexpr int kQStages = 2;                              // 4 KiB stages per warp: 32 KiB per CTA
 
 // 16-byte asynchronous copy global -> shared (L2 only); src_bytes = 0 fills
 // the 16 bytes with zeros without reading.
@@ -258,8 +258,12 @@ __device__ __noinline__ void q_group_huge(const unsigned char *row, int lane, fl
     }
 }
 
-// The codes (kBits = 4: SMOE-Q4, 2: SMOE-Q2) of one group of 64 weights (32
-// bf16 pairs in u), its scale and bias.  Per pair of weights, in packed fp32:
+// The codes (kBits = 4: SMOE-Q4, 2: SMOE-Q2) of one group of 64 weights, its
+// scale and bias.  `row` is the lane's group in its swizzled shared-memory row
+// (chunk c of 8 weights at ((c ^ lane) & 7) * 16); it is read twice, once for
+// the least and greatest weight and once for the codes, so that no more than
+// one code word's weights are held in registers.  Per pair of weights, in
+// packed fp32:
 //   d  = RN(w kk - mn kk)              (kk = 1, or 2^64 for a scale below 2^-62:
 //                                       a power of two, so every value stays exact)
 //   c  = RN(d r + 2^23)                 r = RN(1 / (s kk)): c holds 2^23 + q0,
@@ -267,26 +271,33 @@ __device__ __noinline__ void q_group_huge(const unsigned char *row, int lane, fl
 //   e  = RN(d r - q0)                   the distance from q0 in scale units
 //   t  = RN(e e - (1/4 - 2^-17))        t >= 0 only near a midpoint
 // d r is within 2^-19 of the exact (w - mn) / s, so a weight with |e| below
-// 1/2 - 2^-17 has q0 as its one nearest level; a pair with t >= 0 in either
-// weight (an exact tie, or a weight within 2^-17 of a midpoint) has both codes
-// re-decided exactly (exact_cbits) in a branch that real weights take for
-// about one weight in 600.  The n = 32 / kBits words e_k of a code word
-// combine into sum_k q_k 2^(kBits k) as (sum_k e_k 2^(kBits k)) minus
-// 0x4B000000 * sum_k 2^(kBits k) (mod 2^32), one shift-add each.  A group
-// whose scale is above 2^120 is coded by q_group_huge, which writes the codes
-// itself (returns true).
+// 1/2 - 2^-17 has q0 as its one nearest level.  The sign of t of both weights
+// of each pair goes into a 32-bit mask; after the pass, each pair whose mask
+// bit is clear (an exact tie or a weight within 2^-17 of a midpoint: about one
+// pair in 250 for real weights) has its two codes re-decided exactly
+// (exact_cbits) and patched into its code word.  The n = 32 / kBits words e_k
+// of a code word combine into sum_k q_k 2^(kBits k) as
+// (sum_k e_k 2^(kBits k)) minus 0x4B000000 * sum_k 2^(kBits k) (mod 2^32), one
+// shift-add each.  A group whose scale is above 2^120 is coded by
+// q_group_huge, which writes the codes itself (returns true).
 template <int kBits>
-__device__ __forceinline__ bool q_group(const uint32_t (&u)[32], const unsigned char *row, int lane,
-                                        uint32_t (&code)[2 * kBits], uint16_t &sb, uint16_t &bb,
-                                        uint32_t *out) {
+__device__ __forceinline__ bool q_group(const unsigned char *row, int lane, uint32_t (&code)[2 * kBits],
+                                        uint16_t &sb, uint16_t &bb, uint32_t *out) {
     constexpr int kWords = 2 * kBits, kPairs = 16 / kBits;  // code words; bf16 pairs per code word
     constexpr uint32_t kPackBias = kBits == 4 ? 0xFB000000u : 0xE7000000u;   // 0x4B000000 * 0x11111111 / 0x55555555
     constexpr float kLevels = (float)((1 << kBits) - 1);
-    uint32_t mn2 = u[0], mx2 = u[0];
+    auto chunk = [&](int c) { return *reinterpret_cast<const uint4 *>(row + ((c ^ lane) & 7) * 16); };
+    uint32_t mn2, mx2;
+    {
+        const uint4 v = chunk(0);
+        mn2 = bf16x2_min(bf16x2_min(v.x, v.y), bf16x2_min(v.z, v.w));
+        mx2 = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
+    }
 #pragma unroll
-    for (int k = 1; k < 32; ++k) {
-        mn2 = bf16x2_min(mn2, u[k]);
-        mx2 = bf16x2_max(mx2, u[k]);
+    for (int c = 1; c < 8; ++c) {
+        const uint4 v = chunk(c);
+        mn2 = bf16x2_min(mn2, bf16x2_min(bf16x2_min(v.x, v.y), bf16x2_min(v.z, v.w)));
+        mx2 = bf16x2_max(mx2, bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w)));
     }
     const float mn = fminf(__uint_as_float(mn2 << 16), __uint_as_float(mn2 & 0xFFFF0000u));
     const float mx = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
@@ -310,26 +321,49 @@ __device__ __forceinline__ bool q_group(const uint32_t (&u)[32], const unsigned 
     const float2 k2 = make_float2(kk, kk), nmn2 = make_float2(-mnk, -mnk), r2 = make_float2(r, r);
     const float2 m23 = make_float2(8388608.0f, 8388608.0f);
     const float2 ntie = make_float2(-(0.25f - 0x1p-17f), -(0.25f - 0x1p-17f));
+    uint32_t clear = 0;            // bit 31 - n: pair n (in processing order) is clear of every midpoint
 #pragma unroll
     for (int k = 0; k < kWords; ++k) {
+        uint32_t u[kPairs];
+#pragma unroll
+        for (int h = 0; h < kPairs / 4; ++h) {
+            const uint4 v = chunk(k * (kPairs / 4) + h);
+            u[4 * h] = v.x;
+            u[4 * h + 1] = v.y;
+            u[4 * h + 2] = v.z;
+            u[4 * h + 3] = v.w;
+        }
         uint32_t acc = 0;
 #pragma unroll
         for (int j = kPairs - 1; j >= 0; --j) {             // elements 2j+1, 2j of the word, highest first
-            const uint32_t p = u[kPairs * k + j];
-            const float2 w = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
-            const float2 d = ffma2(w, k2, nmn2);
+            const uint32_t p = u[j];
+            const float2 d = ffma2(make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)), k2, nmn2);
             const float2 c = ffma2(d, r2, m23);
             const float2 e = ffma2(d, r2, fsub2(m23, c));    // m23 - c = -q0 exactly
             const float2 t = ffma2(e, e, ntie);
-            uint32_t cx = __float_as_uint(c.x), cy = __float_as_uint(c.y);
-            if (__builtin_expect((int)(__float_as_uint(t.x) & __float_as_uint(t.y)) >= 0, 0)) {
-                cx = exact_cbits(__fmul_rn(w.x, kk), mnk, sk, cx);
-                cy = exact_cbits(__fmul_rn(w.y, kk), mnk, sk, cy);
-            }
-            acc = (acc << kBits) + cy;
-            acc = (acc << kBits) + cx;
+            clear = (clear << 1) + ((__float_as_uint(t.x) & __float_as_uint(t.y)) >> 31);
+            acc = (acc << kBits) + __float_as_uint(c.y);
+            acc = (acc << kBits) + __float_as_uint(c.x);
         }
         code[k] = acc - kPackBias;
+    }
+    // the pairs near a midpoint, decided exactly
+    for (uint32_t fl = ~clear; fl != 0;) {
+        const int n = __clz(fl);
+        fl &= ~(0x80000000u >> n);
+        const int k = n / kPairs, j = kPairs - 1 - n % kPairs, pi = kPairs * k + j;   // pair: elements 2pi, 2pi+1
+        const uint32_t p = *reinterpret_cast<const uint32_t *>(row + (((pi >> 2) ^ lane) & 7) * 16 + (pi & 3) * 4);
+        const float wx = __uint_as_float(p << 16), wy = __uint_as_float(p & 0xFFFF0000u);
+        const uint32_t cx = exact_cbits(__fmul_rn(wx, kk), mnk, sk,
+                                        __float_as_uint(__fmaf_rn(__fmaf_rn(wx, kk, -mnk), r, 8388608.0f)));
+        const uint32_t cy = exact_cbits(__fmul_rn(wy, kk), mnk, sk,
+                                        __float_as_uint(__fmaf_rn(__fmaf_rn(wy, kk, -mnk), r, 8388608.0f)));
+        const int sh = 2 * kBits * j;
+        const uint32_t field = ((cx - 0x4B000000u) | ((cy - 0x4B000000u) << kBits)) << sh;
+        const uint32_t msk = ((1u << (2 * kBits)) - 1u) << sh;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w)
+            if (w == k) code[w] = (code[w] & ~msk) | field;
     }
     return false;
 }
@@ -369,21 +403,12 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         cp_async_wait<kQStages - 1>();                       // this lane's copies of step i landed
         __syncwarp();                                        // ... and every other lane's
         const unsigned char *stage = ring[warp][i % kQStages];
-        uint32_t u[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(stage + lane * 128 + ((c ^ lane) & 7) * 16);
-            u[4 * c] = v.x;
-            u[4 * c + 1] = v.y;
-            u[4 * c + 2] = v.z;
-            u[4 * c + 3] = v.w;
-        }
         const long long grp = (st0 + i * warps) * 32 + lane;
         const bool live = grp < n_groups;
         uint32_t code[2 * kBits];
         uint16_t sb, bb;
         uint32_t *cq = reinterpret_cast<uint32_t *>(codes + (live ? grp : 0) * (8 * kBits));
-        const bool exact = q_group<kBits>(u, stage + lane * 128, lane, code, sb, bb, live ? cq : nullptr);
+        const bool exact = q_group<kBits>(stage + lane * 128, lane, code, sb, bb, live ? cq : nullptr);
         if (live) {
             if (!exact) {
 #pragma unroll
