@@ -128,7 +128,8 @@ class Clocks:
 
 def traffic_from_profile(name, source_files, key="traffic_bytes_per_layer"):
     """DRAM bytes recorded under `key` in profiles/<name>.md, if the kernels it
-    was taken on are unchanged (sha256 of their sources matches)."""
+    was taken on are unchanged (sha256 of their sources' code, comments
+    stripped, matches the digest recorded with the capture)."""
     path = os.path.join(ROOT, "profiles", name + ".md")
     if not os.path.exists(path):
         return None
@@ -142,10 +143,18 @@ def traffic_from_profile(name, source_files, key="traffic_bytes_per_layer"):
     return float(m.group(1))
 
 
+def _code_only(text):
+    """Source text without comments and blank space: the digest then changes
+    when the code changes, not when a comment does."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def source_digest(source_files):
     cur = hashlib.sha256()
     for f in source_files:
-        cur.update(open(os.path.join(ROOT, f), "rb").read())
+        cur.update(_code_only(open(os.path.join(ROOT, f)).read()).encode())
     return cur.hexdigest()
 
 
@@ -317,9 +326,19 @@ def calibrate_alpha(smoe, synth, L0, dev, lo=0.0, hi=0.95, target=(60, 100)):
     return a, u
 
 
-def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
-    """Layer-major prefill over the 235B stack: each 64-token chunk goes
-    through all layers (per layer: route, union, grouped FFN, combine)."""
+def union_sizes(idx):
+    """Distinct experts per row of idx [..., T, K] (the chunk's union size)."""
+    flat = idx.reshape(-1, idx.shape[-2] * idx.shape[-1])
+    srt, _ = torch.sort(flat, dim=1)
+    return 1 + (srt[:, 1:] != srt[:, :-1]).sum(dim=1).reshape(idx.shape[:-2])
+
+
+def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha, hbm_peak=None, code_bits=4):
+    """Layer-major prefill over the stack: each 64-token chunk goes through all
+    layers (per layer: route, union, grouped FFN, combine), replayed from CUDA
+    graphs.  After the timed replays, one untimed pass records every layer's
+    top-k ids per chunk, from which the union sizes U follow; the algorithmic
+    bytes are sum over chunks and layers of U x expert bytes + router bytes."""
     res = {}
     T = 64
     ws = stack.ws
@@ -327,14 +346,19 @@ def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
     bufs = [torch.empty((T, stack.D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     idx = torch.empty((T, K), dtype=torch.int32, device=dev)
 
-    def chunk(t):
+    def chunk(t, idx_all=None):
         cur = xa[:t]
         for i, L in enumerate(stack.L):
             nxt = bufs[i % 2][:t]
-            smoe.smoe_moe_prefill_chunk(L, cur, t, nxt, idx_out=idx[:t] if i == 0 else None, ws=ws)
+            io = idx[:t] if i == 0 else None
+            if idx_all is not None:
+                io = idx_all[i, :t]
+            smoe.smoe_moe_prefill_chunk(L, cur, t, nxt, idx_out=io, ws=ws)
             cur = nxt
 
     graphs = {T: capture(lambda: chunk(T))}
+    eb = expert_bytes(stack.D, stack.F, code_bits)
+    rb = E * stack.D * 2
     for n in prompt_lens:
         x = synth.correlated_hidden(n, stack.D, alpha, seed=SEED + n, device=dev)
         tail = n % T
@@ -350,9 +374,127 @@ def time_prefill(stack, smoe, synth, dev, prompt_lens, alpha):
         ev1.record()
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1)
-        res[str(n)] = {"ms": round(ms, 3), "tok_s": round(n / ms * 1e3, 1),
-                       "chunks": (n + T - 1) // T}
+        # untimed pass: every layer's ids for every chunk -> union sizes
+        us = []
+        idx_all = torch.empty((stack.n, T, K), dtype=torch.int32, device=dev)
+        for c0 in range(0, n, T):
+            t = min(T, n - c0)
+            xa[:t].copy_(x[c0:c0 + t])
+            chunk(t, idx_all)
+            us.append(union_sizes(idx_all[:, :t]))
+        U = torch.stack(us).cpu()                          # [chunks, layers]
+        nbytes = int(U.sum()) * eb + U.numel() * rb
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[str(n)] = {"ms": round(ms, 3), "tok_s": round(n / ms * 1e3, 1), "chunks": (n + T - 1) // T,
+                       "union_mean": round(float(U.float().mean()), 2), "union_min": int(U.min()),
+                       "union_max": int(U.max()), "union_layer0": [int(u) for u in U[:, 0]][:8],
+                       "bytes": nbytes, "gbs": round(gbs, 1)}
+        if hbm_peak:
+            res[str(n)]["frac"] = round(gbs / hbm_peak, 4)
     return res
+
+
+def time_skewed(stack, smoe, synth, dev, hbm_peak, alpha):
+    """The skewed-routing workload on the 30B shape.  Prefill: 16 chunks of 64
+    tokens whose layer-0 router logits carry a Zipf(1.2) bias over a seeded
+    expert permutation (x_t = z_t + pinv(Wr) b, the bias scale raised until the
+    largest bucket of a chunk holds 30-60 tokens), through layer 0 -- the layer
+    the bias is realised at -- beside 16 chunks whose tokens share a direction
+    (alpha as calibrated for the 60-100 expert unions) through the same layer;
+    each set replayed from one CUDA graph.  Hot experts of the Zipf chunks recur
+    from chunk to chunk, so L2 may keep them: the GB/s are algorithmic bytes
+    over time, not DRAM traffic.  Decode: a stream whose consecutive tokens
+    share about 46 % of their layer-0 experts (x_{s+1} = rho x_s + sqrt(1 -
+    rho^2) z), through the 48-layer stack."""
+    L0, W0 = stack.L[0], stack.W[0]
+    T, NCH = 64, 16
+    ws = smoe.workspace(L0, T)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    scale = None
+    for sc in (1.0, 1.5, 2.0, 3.0, 4.0, 6.0):
+        x = synth.zipf_bias_hidden(T, W0.router_w.float(), 1.2, sc, seed=SEED)
+        smoe.smoe_route_topk(L0, x, T, idx, w, ws=ws)
+        if 30 <= int(torch.bincount(idx.flatten().long(), minlength=E).max()) <= 60:
+            scale = sc
+            break
+    out = {"zipf_s": 1.2, "bias_scale": scale}
+    eb, rb = expert_bytes(stack.D, stack.F), E * stack.D * 2
+    sets = {"zipf": torch.stack([synth.zipf_bias_hidden(T, W0.router_w.float(), 1.2, scale or 6.0,
+                                                        seed=SEED + c) for c in range(NCH)]),
+            "uniform": torch.stack([synth.correlated_hidden(T, stack.D, alpha, seed=SEED + 100 + c,
+                                                            device=dev) for c in range(NCH)])}
+    for name, xs in sets.items():
+        ys = torch.empty_like(xs)
+        ids = torch.empty((NCH, T, K), dtype=torch.int32, device=dev)
+
+        def run():
+            for c in range(NCH):
+                smoe.smoe_moe_prefill_chunk(L0, xs[c], T, ys[c], idx_out=ids[c], ws=ws)
+
+        g = capture(run)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = 8
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * NCH)
+        U = union_sizes(ids)
+        bmax = [int(torch.bincount(ids[c].flatten().long(), minlength=E).max()) for c in range(NCH)]
+        nb = float(U.float().mean()) * eb + rb
+        out[name] = {"us_per_chunk": round(ms * 1e3, 2), "tok_s": round(T / ms * 1e3, 1),
+                     "union_mean": round(float(U.float().mean()), 2),
+                     "largest_bucket_mean": round(sum(bmax) / NCH, 2), "largest_bucket_max": max(bmax),
+                     "bytes_per_chunk": int(nb), "gbs": round(nb / (ms / 1e3) / 1e9, 1),
+                     "frac": round(nb / (ms / 1e3) / 1e9 / hbm_peak, 4)}
+        del g
+    # decode stream with ~46 % adjacent overlap at layer 0 (rho picked on the GPU router)
+    best = None
+    i1 = torch.empty((64, K), dtype=torch.int32, device=dev)
+    w1 = torch.empty((64, K), dtype=torch.float32, device=dev)
+    for rho in (0.5, 0.6, 0.7, 0.75, 0.8, 0.85, 0.9):
+        st = synth.overlap_stream(64, stack.D, rho, seed=SEED + 7, device=dev)
+        smoe.smoe_route_topk(L0, st, 64, i1, w1, ws=ws)
+        a = i1.cpu().tolist()
+        ov = sum(len(set(p) & set(q)) / K for p, q in zip(a[:-1], a[1:])) / 63
+        if best is None or abs(ov - 0.46) < abs(best[1] - 0.46):
+            best = (rho, ov)
+    rho, ov = best
+    stream = synth.overlap_stream(256, stack.D, rho, seed=SEED + 8, device=dev)
+    ms_tok, _ = time_decode(stack, stream, 256, 16, 16)        # tokens in stream order
+    out["decode_stream"] = {"rho": rho, "layer0_adjacent_overlap": round(ov, 3),
+                            "tok_s": round(1e3 / ms_tok, 2), "ms_per_token": round(ms_tok, 4)}
+    return out
+
+
+def near_tie_count(stack, smoe, states, n_tokens):
+    """Routing near-ties that n_tokens decode tokens meet through the stack: a
+    (token, layer) where two adjacent logits among the top k+1 lie within
+    tau = 64 * 2^-24 * max_e sum_d |Wr[e][d] xn[d]| (the GPU's fp32 logits and
+    normed input), where fp32 and fp64 may rank experts differently."""
+    dev = states.device
+    idx = torch.empty(K, dtype=torch.int32, device=dev)
+    w = torch.empty(K, dtype=torch.float32, device=dev)
+    lg = torch.empty(E, dtype=torch.float32, device=dev)
+    xn = torch.empty(stack.D, dtype=torch.bfloat16, device=dev)
+    count = 0
+    for t in range(n_tokens):
+        cur = states[t].clone()
+        nxt = torch.empty_like(cur)
+        for Wl, L in zip(stack.W, stack.L):
+            smoe.smoe_route_topk(L, cur, 1, idx, w, logits=lg, xn=xn, ws=stack.ws)
+            tau = 64 * 2.0 ** -24 * float((Wl.router_w.double().abs() @ xn.double().abs()).max())
+            top = torch.topk(lg.double(), K + 1).values
+            count += int(bool(((top[:-1] - top[1:]) < tau).any()))
+            smoe.smoe_moe_decode(L, cur, nxt, ws=stack.ws)
+            cur, nxt = nxt, cur
+    torch.cuda.synchronize()
+    return {"tokens": n_tokens, "layers": stack.n, "token_layers_with_near_tie": count}
 
 
 def time_dense(smoe, synth, dev, hbm_peak):
@@ -440,9 +582,8 @@ def cpu_baseline_oracle(stack, states, n_tokens, n_layers):
     is scaled to the full stack depth."""
     import numpy as np
     from oracle import oracle
-    from tests.util import oracle_layer
     oracle.build()
-    OL = [oracle_layer(w) for w in stack.W[:n_layers]]
+    OL = [oracle.layer_from_weights(w) for w in stack.W[:n_layers]]
     x = states[:n_tokens].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
     cur = x
@@ -587,7 +728,13 @@ def our_arm(args):
         # prefill on the 30B shape, SMOE-Q4 here and SMOE-Q2 below (same prompts, same router draw)
         alpha30, u30 = calibrate_alpha(smoe, synth, stack.L[0], dev)
         pre30 = {"alpha": round(alpha30, 4), "layer0_union_64tok": u30,
-                 "q4": time_prefill(stack, smoe, synth, dev, [512, 4096], alpha30)}
+                 "q4": time_prefill(stack, smoe, synth, dev, [512, 4096], alpha30, hbm_peak)}
+        log("[bench] skewed routing (Zipf chunks, overlapping decode stream)")
+        line["skewed_routing"] = dict(
+            workload="30B shape: 16 Zipf(1.2)-biased 64-token chunks through layer 0 beside 16 "
+                     "direction-sharing chunks; a 46 %-overlap decode stream through 48 layers",
+            **time_skewed(stack, smoe, synth, dev, hbm_peak, alpha30))
+        line["near_ties"] = near_tie_count(stack, smoe, states, 8)
     del stack
     torch.cuda.empty_cache()
 
@@ -603,10 +750,13 @@ def our_arm(args):
                              "effective_gbs": round(bq2 / (msq2 / 1e3) / 1e9, 1),
                              "bytes_per_token": bq2}
         alpha_q2, u_q2 = calibrate_alpha(smoe, synth, q2.L[0], dev)
-        pre30["q2"] = time_prefill(q2, smoe, synth, dev, [512, 4096], alpha_q2)
+        pre30["q2"] = time_prefill(q2, smoe, synth, dev, [512, 4096], alpha_q2, hbm_peak, code_bits=2)
         pre30["q2_alpha"], pre30["q2_layer0_union_64tok"] = round(alpha_q2, 4), u_q2
         line["prefill_30b"] = dict(workload="30B-shaped 48-layer layer-major prefill, chunks of 64, "
                                             "SMOE-Q4 and SMOE-Q2 stacks", **pre30)
+        line["prefill_30b"]["roofline_4096"] = {
+            "bound": "hbm", "bytes": "sum over chunks and layers of union size x expert bytes + router bytes",
+            "q4_frac": pre30["q4"]["4096"]["frac"], "q2_frac": pre30["q2"]["4096"]["frac"]}
         del q2
         torch.cuda.empty_cache()
         log("[bench] dense matvec and quantiser")
@@ -618,16 +768,35 @@ def our_arm(args):
         st235 = synth.hidden(128, D235, seed=SEED + 1, device=dev)
         ms235, _ = time_decode(big, st235, 128, 16, 16)
         b235 = L235 * (K * expert_bytes(D235, F235) + E * D235 * 2)
+        ach235 = b235 / (ms235 / 1e3) / 1e9
+        ffn235 = time_ffn(big, st235, 4)
+        fb235 = K * expert_bytes(D235, F235)
         line["decode_235b"] = {"workload": "235B-shaped 94-layer MoE decode, batch 1 (d_model "
                                            "4096, ffn 1536), 128 tokens",
                                "tok_s": round(1e3 / ms235, 2), "ms_per_token": round(ms235, 4),
                                "us_per_layer": round(ms235 * 1e3 / L235, 2),
-                               "effective_gbs": round(b235 / (ms235 / 1e3) / 1e9, 1)}
+                               "effective_gbs": round(ach235, 1),
+                               "roofline": {"bound": "hbm", "achieved": round(ach235, 1), "peak": hbm_peak,
+                                            "unit": "GB/s", "frac": round(ach235 / hbm_peak, 4),
+                                            "kernel": "k_decode_layer, one launch per token over 94 layers",
+                                            "bytes_per_launch": b235, "ms_per_launch": round(ms235, 5)},
+                               "ffn_call": {"kernel": "k_decode_layer (FFN only), 8 experts of 10,616,832 B",
+                                            "bytes": fb235, "ms": round(ffn235, 5),
+                                            "gbs": round(fb235 / (ffn235 / 1e3) / 1e9, 1),
+                                            "frac": round(fb235 / (ffn235 / 1e3) / 1e9 / hbm_peak, 4)}}
         alpha, u0 = calibrate_alpha(smoe, synth, big.L[0], dev)
-        pre = time_prefill(big, smoe, synth, dev, [45, 512, 4096], alpha)
+        pre = time_prefill(big, smoe, synth, dev, [45, 512, 4096], alpha, hbm_peak)
         line["prefill"] = {"workload": "235B-shaped 94-layer layer-major prefill, chunks of 64",
                            "alpha": round(alpha, 4), "layer0_union_64tok": u0, "prompts": pre,
-                           "tok_s_4096": pre["4096"]["tok_s"]}
+                           "tok_s_4096": pre["4096"]["tok_s"],
+                           "roofline_4096": {"bound": "hbm", "achieved": pre["4096"]["gbs"], "peak": hbm_peak,
+                                             "unit": "GB/s", "frac": pre["4096"]["frac"],
+                                             "bytes": pre["4096"]["bytes"],
+                                             "bytes_rule": "sum over chunks and layers of union size x "
+                                                           "10,616,832 B + router 1,048,576 B",
+                                             "time": "whole chunk path (route, union, gather, gate/up and "
+                                                     "down grouped GEMMs, combine), CUDA events around "
+                                                     "graph replays"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_ > 1:
@@ -647,7 +816,6 @@ def reference_arm(args):
     import numpy as np
     from oracle import oracle
     from quantised_expert_ffn_gb300 import synth
-    from tests.util import oracle_layer
     oracle.build()
     # bounded run: past 128 steps (warm-up included) fewer layers per step, never fewer
     # tokens (the tokens are what the oracle spreads over the host cores)
@@ -656,7 +824,7 @@ def reference_arm(args):
         n_layers = max(1, n_layers * 128 // (args.steps + args.warmup))
     W = [synth.layer_weights(D30, E, F30, K, seed=SEED * 1000 + i, device="cpu", rms_norm=True)
          for i in range(n_layers)]
-    OL = [oracle_layer(w) for w in W]
+    OL = [oracle.layer_from_weights(w) for w in W]
     states = synth.hidden(256, D30, seed=SEED, device="cpu")
     x_all = states.contiguous().view(torch.int16).numpy().view(np.uint16)
     ntok = args.cpu_tokens
