@@ -463,6 +463,12 @@ def test_alternate_engines_in_subprocess(smoe):
                         "tests/test_gpu_parity.py", "-k", "(prefill or decode) and not subprocess"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    # the per-slot expert outputs and the quantiser-written weights on the same engines
+    # (SMOE-Q2 and the fp16-range case skip there: those engines are SMOE-Q4 and fp32)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+                        "tests/test_gpu_prefill_ffn.py"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
 # ------------------------------------------------------------- skewed routing
