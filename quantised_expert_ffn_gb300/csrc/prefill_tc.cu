@@ -17,13 +17,18 @@
 //               memory, turn them into fp16 w = s*q + b (one rounding; exact
 //               when b = -8 s, since s*(q-8) needs at most 11 bits) and store
 //               them straight into tensor memory (tcgen05.st): warp w owns
-//               TMEM lanes 32*(w%4).. = tile rows, and K half w/4 of each chunk;
+//               TMEM lanes 32*(w%4).. = tile rows, and the chunks of parity
+//               w/4, so the two dequant warps of a scheduler work on alternate
+//               chunks and one's waits overlap the other's arithmetic;
 //   warp 12     TMA: codes tiles (no swizzle) and the bucket's activation
 //               tile (128-byte swizzle) into a ring of shared-memory stages;
-//   warp 13     MMA: one thread issues tcgen05.mma with A from tensor memory
-//               (M=128 weight rows, K=16) and B from shared memory (N =
+//   warps 13-14 MMA: one thread of each issues tcgen05.mma with A from tensor
+//               memory (M=128 weight rows, K=16) and B from shared memory (N =
 //               pad16(bucket) tokens), fp16 x fp16 -> fp32 in TMEM, and commits
-//               stages back;
+//               stages back -- warp 13 the gate (or down) matrix, warp 14 the up
+//               matrix.  A thread blocks on each tcgen05.mma until the tensor
+//               pipe takes it; two issuing threads keep the pipe fed while
+//               either one waits on a barrier or commits;
 //   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
@@ -53,11 +58,12 @@ namespace smoe {
 
 namespace {
 
-constexpr int kTcThreads = 448;
+constexpr int kTcThreads = 480;
 constexpr int kProdThreads = 256;    // warps 0-7
 constexpr int kEpiWarp0 = 8;         // warps 8-11
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;
+constexpr int kMma2Warp = 14;      // gate/up: the up matrix's MMA thread
 constexpr int kTile = 128;
 constexpr int kKc = 64;
 constexpr int kNmax = 64;
@@ -189,14 +195,16 @@ __device__ __forceinline__ void mma_chunk_ta(uint32_t d, uint32_t a, uint64_t b0
         : "memory");
 }
 
-// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[4][4]) {
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[8][4]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
-        " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0][0]), "r"(r[0][1]), "r"(r[0][2]), "r"(r[0][3]), "r"(r[1][0]), "r"(r[1][1]), "r"(r[1][2]),
-        "r"(r[1][3]), "r"(r[2][0]), "r"(r[2][1]), "r"(r[2][2]), "r"(r[2][3]), "r"(r[3][0]), "r"(r[3][1]),
-        "r"(r[3][2]), "r"(r[3][3])
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+        " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0][0]), "r"(r[0][1]), "r"(r[0][2]), "r"(r[0][3]), "r"(r[1][0]), "r"(r[1][1]), "r"(r[1][2]), "r"(r[1][3]),
+        "r"(r[2][0]), "r"(r[2][1]), "r"(r[2][2]), "r"(r[2][3]), "r"(r[3][0]), "r"(r[3][1]), "r"(r[3][2]), "r"(r[3][3]),
+        "r"(r[4][0]), "r"(r[4][1]), "r"(r[4][2]), "r"(r[4][3]), "r"(r[5][0]), "r"(r[5][1]), "r"(r[5][2]), "r"(r[5][3]),
+        "r"(r[6][0]), "r"(r[6][1]), "r"(r[6][2]), "r"(r[6][3]), "r"(r[7][0]), "r"(r[7][1]), "r"(r[7][2]), "r"(r[7][3])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -223,12 +231,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // ---- dequant ---------------------------------------------------------------
-
-// bf16 element j (runtime, 0..7) of 8 packed in a uint4, as a float.
-__device__ __forceinline__ float pick_f(const uint4 &v, int j) {
-    const uint32_t w = (j & 4) ? ((j & 2) ? v.w : v.z) : ((j & 2) ? v.y : v.x);
-    return bf16_to_f32((j & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xFFFFu));
-}
 
 __device__ __forceinline__ __half2 f2h2(float f) { return __half2half2(__float2half_rn(f)); }
 
@@ -307,23 +309,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *afull = empty + kStages;        // [kStages] dequantised A written
     uint64_t *accfull = afull + kStages;      // [2]
     uint64_t *accempty = accfull + 2;         // [2]
-    uint64_t *drain = accempty + 2;           // [1] all issued MMAs complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *drain = accempty + 2;           // [2] all MMAs issued by MMA thread i complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    // A chunk is dequantised by the 4 warps of its parity (128 threads) and
+    // multiplied by one MMA thread per matrix, each committing on its own.
+    constexpr uint32_t kIssuers = kPair ? 2 : 1;
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kProdThreads + 1);
+            mbar_init(&empty[i], kProdThreads / 2 + kIssuers);
         }
-        for (int i = 0; i < kStages; ++i) mbar_init(&afull[i], kProdThreads);
+        for (int i = 0; i < kStages; ++i) mbar_init(&afull[i], kProdThreads / 2);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&accfull[i], 1);
+            mbar_init(&accfull[i], kIssuers);
             mbar_init(&accempty[i], 128);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -374,8 +380,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (uint32_t k = (g > (uint32_t)kStages ? g - kStages : 0); k < g; ++k)
                 mbar_wait(&full[k % kStages], (k / kStages) & 1, abort_flag, p.status);
         }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+    } else if (warp == kMmaWarp || warp == kMma2Warp) {
+        const int mat = warp - kMmaWarp;          // 0: gate (or down), 1: up
+        if (lane == 0 && (mat == 0 || kPair)) {
             uint32_t g = 0, i = 0;
             bool issued = false;
             for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
@@ -401,8 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t acol = tmem + kACol0 + a * S::kMats * kACols;
                     const uint64_t bd = smem_desc_sw128(smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes));
                     const uint32_t acc = c > 0 ? 1u : 0u;
-                    mma_chunk_ta(d0, acol, bd, idesc, acc);
-                    if (kPair) mma_chunk_ta(d0 + kUpCol, acol + kACols, bd, idesc, acc);
+                    mma_chunk_ta(d0 + mat * kUpCol, acol + mat * kACols, bd, idesc, acc);
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
@@ -410,109 +416,140 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // every issued MMA must be complete before the TMEM is released
             if (issued) {
-                mma_commit(drain);
-                mbar_wait(drain, 0, abort_flag, p.status);
+                mma_commit(&drain[mat]);
+                mbar_wait(&drain[mat], 0, abort_flag, p.status);
             }
         }
     } else if (warp < 8) {
         // ---------------- dequant producers ----------------
-        // warp w writes TMEM lanes 32*(w%4).. (its quarter): row r of the tile,
-        // K half h of each chunk (columns 16h..16h+15 of the matrix's 32)
-        const int r = 32 * (warp & 3) + lane, h = warp >> 2;
-        const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
-        uint32_t g = 0;
-        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x) {
+        // warp w writes TMEM lanes 32*(w%4).. (its quarter of the tile's rows)
+        // for the chunks of parity w/4, the chunk's full 64 codes of each matrix;
+        // the two warps of a scheduler thus work on alternate chunks, and one's
+        // waits overlap the other's arithmetic.
+        const int rq = warp & 3, cp = warp >> 2;
+        const int r = 32 * rq + lane;
+        const uint32_t tlane = (uint32_t)(32 * rq) << 16;
+        constexpr float kLv = kQ2 ? 3.f : 15.f;
+        uint32_t gbase = 0;     // global index of the current unit's chunk 0
+        // Chunk c of the unit: wait for its stage, turn the codes into fp16 s*q + b
+        // and store them into the stage's A columns.  false when a wait gave up.
+        auto chunk = [&](int c, float s0f, float b0f, float s1f, float b1f) -> bool {
+            const uint32_t g = gbase + (uint32_t)c;
+            const int s = g % kStages, a = s;
+            if (!levels_in_fp16(s0f, b0f, kLv) || !levels_in_fp16(s1f, b1f, kLv))
+                set_status(p.status, SMOE_ERR_RANGE);
+            const __half2 s0 = f2h2(s0f), b0 = f2h2(b0f), s1 = f2h2(s1f), b1 = f2h2(b1f);
+            // waits are warp-uniform: the TMEM store below is warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)))
+                return false;
+            const unsigned char *stg = st_ring + s * S::kStageBytes;
+            uint32_t q0[8][4], q1[8][4];
+            if constexpr (kQ2) {                      // 16 bytes per row
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 16);
+                uint4 c1 = c0;
+                if (kPair) c1 = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 16);
+                mbar_arrive(&empty[s]);               // codes consumed
+                dequant_word_q2(c0.x, s0, b0, q0[0], q0[1]);
+                dequant_word_q2(c0.y, s0, b0, q0[2], q0[3]);
+                dequant_word_q2(c0.z, s0, b0, q0[4], q0[5]);
+                dequant_word_q2(c0.w, s0, b0, q0[6], q0[7]);
+                if (kPair) {
+                    dequant_word_q2(c1.x, s1, b1, q1[0], q1[1]);
+                    dequant_word_q2(c1.y, s1, b1, q1[2], q1[3]);
+                    dequant_word_q2(c1.z, s1, b1, q1[4], q1[5]);
+                    dequant_word_q2(c1.w, s1, b1, q1[6], q1[7]);
+                }
+            } else {                                  // 32 bytes per row
+                const uint4 c0a = *reinterpret_cast<const uint4 *>(stg + r * 32);
+                const uint4 c0b = *reinterpret_cast<const uint4 *>(stg + r * 32 + 16);
+                uint4 c1a = c0a, c1b = c0b;
+                if (kPair) {
+                    c1a = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32);
+                    c1b = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + 16);
+                }
+                mbar_arrive(&empty[s]);               // codes consumed
+                dequant_word(c0a.x, s0, b0, q0[0]);
+                dequant_word(c0a.y, s0, b0, q0[1]);
+                dequant_word(c0a.z, s0, b0, q0[2]);
+                dequant_word(c0a.w, s0, b0, q0[3]);
+                dequant_word(c0b.x, s0, b0, q0[4]);
+                dequant_word(c0b.y, s0, b0, q0[5]);
+                dequant_word(c0b.z, s0, b0, q0[6]);
+                dequant_word(c0b.w, s0, b0, q0[7]);
+                if (kPair) {
+                    dequant_word(c1a.x, s1, b1, q1[0]);
+                    dequant_word(c1a.y, s1, b1, q1[1]);
+                    dequant_word(c1a.z, s1, b1, q1[2]);
+                    dequant_word(c1a.w, s1, b1, q1[3]);
+                    dequant_word(c1b.x, s1, b1, q1[4]);
+                    dequant_word(c1b.y, s1, b1, q1[5]);
+                    dequant_word(c1b.z, s1, b1, q1[6]);
+                    dequant_word(c1b.w, s1, b1, q1[7]);
+                }
+            }
+            tc_fence_after();      // A stage a: its last MMAs completed before these codes landed
+            const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols;
+            tmem_st32(acol, q0);
+            if (kPair) tmem_st32(acol + kACols, q1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&afull[a]);
+            return true;
+        };
+        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, gbase += NC) {
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
             const int e = p.union_ids[u];
             const size_t row = (size_t)e * p.rows_per_expert + tile * kTile + r;
             const int NG = p.k_dim / kGroup;
-            // Scales and biases of this row: with vec_scales, 8 groups per 16-byte
-            // load, the next 8 requested one block ahead of use.
-            uint4 vs0{}, vb0{}, vs1{}, vb1{}, ns0{}, nb0{}, ns1{}, nb1{};
-            auto load8 = [&](int c8, uint4 &ts0, uint4 &tb0, uint4 &ts1, uint4 &tb1) {
-                const size_t o = row * NG + c8;
-                ts0 = __ldg(reinterpret_cast<const uint4 *>(p.s0 + o));
-                tb0 = __ldg(reinterpret_cast<const uint4 *>(p.b0 + o));
-                if (kPair) {
-                    ts1 = __ldg(reinterpret_cast<const uint4 *>(p.s1 + o));
-                    tb1 = __ldg(reinterpret_cast<const uint4 *>(p.b1 + o));
-                }
-            };
+            bool ok = true;
             if (p.vec_scales) {
+                // Scales and biases of this row, 8 groups per 16-byte load, the
+                // next 8 requested one block ahead of use; of a block's 8 groups
+                // this warp takes those of its chunk parity (the cp-th bf16 of
+                // each 32-bit word).
+                uint4 vs0{}, vb0{}, vs1{}, vb1{}, ns0{}, nb0{}, ns1{}, nb1{};
+                auto load8 = [&](int c8, uint4 &ts0, uint4 &tb0, uint4 &ts1, uint4 &tb1) {
+                    const size_t o = row * NG + c8;
+                    ts0 = __ldg(reinterpret_cast<const uint4 *>(p.s0 + o));
+                    tb0 = __ldg(reinterpret_cast<const uint4 *>(p.b0 + o));
+                    if (kPair) {
+                        ts1 = __ldg(reinterpret_cast<const uint4 *>(p.s1 + o));
+                        tb1 = __ldg(reinterpret_cast<const uint4 *>(p.b1 + o));
+                    }
+                };
+                const int sh = 16 * cp;
+                auto pick = [&](const uint4 &v, int j2) {
+                    const uint32_t w = j2 == 0 ? v.x : j2 == 1 ? v.y : j2 == 2 ? v.z : v.w;
+                    return bf16_to_f32((uint16_t)(w >> sh));
+                };
                 load8(0, vs0, vb0, vs1, vb1);
                 if (NC > 8) load8(8, ns0, nb0, ns1, nb1);
-            }
-            bool ok = true;
-            for (int c = 0; c < NC; ++c, ++g) {
-                const int s = g % kStages, a = s;
-                float s0f, b0f, s1f, b1f;
-                if (p.vec_scales) {
-                    if ((c & 7) == 0 && c > 0) {
+                for (int c8 = 0; c8 < NC && ok; c8 += 8) {
+                    if (c8 > 0) {
                         vs0 = ns0; vb0 = nb0; vs1 = ns1; vb1 = nb1;
-                        if (c + 8 < NC) load8(c + 8, ns0, nb0, ns1, nb1);
+                        if (c8 + 8 < NC) load8(c8 + 8, ns0, nb0, ns1, nb1);
                     }
-                    s0f = pick_f(vs0, c & 7);
-                    b0f = pick_f(vb0, c & 7);
-                    s1f = s0f, b1f = b0f;
-                    if (kPair) {
-                        s1f = pick_f(vs1, c & 7);
-                        b1f = pick_f(vb1, c & 7);
+#pragma unroll
+                    for (int j2 = 0; j2 < 4; ++j2) {
+                        const float s0f = pick(vs0, j2), b0f = pick(vb0, j2);
+                        const float s1f = kPair ? pick(vs1, j2) : s0f, b1f = kPair ? pick(vb1, j2) : b0f;
+                        if (!chunk(c8 + 2 * j2 + cp, s0f, b0f, s1f, b1f)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                } else {
+                }
+            } else {
+                for (int c = cp; c < NC; c += 2) {
                     // scales/biases of this row and group (L1-cached: 16 groups share a sector)
-                    s0f = bf16_to_f32(p.s0[row * NG + c]);
-                    b0f = bf16_to_f32(p.b0[row * NG + c]);
-                    s1f = s0f, b1f = b0f;
-                    if (kPair) {
-                        s1f = bf16_to_f32(p.s1[row * NG + c]);
-                        b1f = bf16_to_f32(p.b1[row * NG + c]);
+                    const float s0f = bf16_to_f32(p.s0[row * NG + c]), b0f = bf16_to_f32(p.b0[row * NG + c]);
+                    const float s1f = kPair ? bf16_to_f32(p.s1[row * NG + c]) : s0f;
+                    const float b1f = kPair ? bf16_to_f32(p.b1[row * NG + c]) : b0f;
+                    if (!chunk(c, s0f, b0f, s1f, b1f)) {
+                        ok = false;
+                        break;
                     }
                 }
-                constexpr float kLv = kQ2 ? 3.f : 15.f;
-                if (!levels_in_fp16(s0f, b0f, kLv) || !levels_in_fp16(s1f, b1f, kLv))
-                    set_status(p.status, SMOE_ERR_RANGE);
-                const __half2 s0 = f2h2(s0f), b0 = f2h2(b0f), s1 = f2h2(s1f), b1 = f2h2(b1f);
-                // waits are warp-uniform: the TMEM store below is warp-collective
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status))) {
-                    ok = false;
-                    break;
-                }
-                const unsigned char *stg = st_ring + s * S::kStageBytes;
-                uint32_t q0[4][4], q1[4][4];
-                if constexpr (kQ2) {                      // 16 bytes per row: half h = 8 bytes, two words
-                    const uint2 c0 = *reinterpret_cast<const uint2 *>(stg + r * 16 + h * 8);
-                    uint2 c1 = c0;
-                    if (kPair) c1 = *reinterpret_cast<const uint2 *>(stg + kCodeBytes + r * 16 + h * 8);
-                    mbar_arrive(&empty[s]);               // codes consumed
-                    dequant_word_q2(c0.x, s0, b0, q0[0], q0[1]);
-                    dequant_word_q2(c0.y, s0, b0, q0[2], q0[3]);
-                    if (kPair) {
-                        dequant_word_q2(c1.x, s1, b1, q1[0], q1[1]);
-                        dequant_word_q2(c1.y, s1, b1, q1[2], q1[3]);
-                    }
-                } else {
-                    const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 32 + h * 16);
-                    uint4 c1 = c0;
-                    if (kPair) c1 = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + h * 16);
-                    mbar_arrive(&empty[s]);               // codes consumed
-                    dequant_word(c0.x, s0, b0, q0[0]);
-                    dequant_word(c0.y, s0, b0, q0[1]);
-                    dequant_word(c0.z, s0, b0, q0[2]);
-                    dequant_word(c0.w, s0, b0, q0[3]);
-                    if (kPair) {
-                        dequant_word(c1.x, s1, b1, q1[0]);
-                        dequant_word(c1.y, s1, b1, q1[1]);
-                        dequant_word(c1.z, s1, b1, q1[2]);
-                        dequant_word(c1.w, s1, b1, q1[3]);
-                    }
-                }
-                tc_fence_after();      // A stage a: its last MMAs completed before these codes landed
-                const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols + h * 16;
-                tmem_st16(acol, q0);
-                if (kPair) tmem_st16(acol + kACols, q1);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&afull[a]);
             }
             if (!ok) break;
         }
