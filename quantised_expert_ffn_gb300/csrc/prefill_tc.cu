@@ -10,9 +10,11 @@
 // tensor cores with the weights as the 128-row M side ("swap AB") and the
 // bucket's tokens as N (padded to a multiple of 16, at most 64).
 //
-// One persistent CTA per SM walks a static list of units (union expert u,
-// 128-row tile); per unit the K dimension is consumed in chunks of 64 (one Q4
-// group).  Warp roles:
+// One persistent CTA per SM walks a static list of units (union expert u and
+// its row tiles: a 128-row tile of both gate and up, or two adjacent 128-row
+// tiles of down, so that every chunk of a unit feeds two MMA threads from one
+// activation tile); per unit the K dimension is consumed in chunks of 64 (one
+// Q4 group).  Warp roles:
 //   warps 0-7   dequant: read the TMA-staged codes of a chunk from shared
 //               memory, turn them into fp16 w = s*q + b (one rounding; exact
 //               when b = -8 s, since s*(q-8) needs at most 11 bits) and store
@@ -84,6 +86,8 @@ struct TcParams {
     int n_tiles;            // 128-row tiles per expert
     int n_chunks;           // K / 64
     int rows_per_expert;    // F (gate/up) or D (down)
+    int tile_rows;          // weight rows of one unit: 128, or 256 for a pair of down tiles
+    int a1_row;             // first row of the second matrix's tile within the unit: 0 (up), 128 (down pair)
     int k_dim;              // K (D or F)
     int out_ld;             // row length of the output (F for h, D for o)
     const int32_t *n_union, *union_ids, *offsets;
@@ -291,7 +295,10 @@ struct Smem {
     static constexpr int kBytes = kBarOff + 1024;   // barriers + tmem slot + flags
 };
 
-template <bool kPair, bool kQ2>
+// kPair: two 128-row A tiles per unit share each chunk's activation tile --
+// gate and up (kHOut: the epilogue writes h = SiLU(g) * u), or two adjacent
+// tiles of the down matrix (the epilogue writes both as fp32 outputs).
+template <bool kPair, bool kQ2, bool kHOut>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int nb = (m + 15) >> 4;            // 1..4
                 const CUtensorMap *tb = nb <= 1 ? &tm_b16 : nb == 2 ? &tm_b32 : nb == 3 ? &tm_b48 : &tm_b64;
                 const uint32_t bbytes = (uint32_t)(nb < 1 ? 1 : nb) * 16 * kKc * 2;  // full box, OOB rows zero-filled
-                const int row = e * p.rows_per_expert + tile * kTile;
+                const int row = e * p.rows_per_expert + tile * p.tile_rows;
                 for (int c = 0; c < NC; ++c, ++g) {
                     const int s = g % kStages;
                     const uint32_t ph = (g / kStages) & 1;
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     constexpr int kCodeRow = kQ2 ? kKc / 4 : kKc / 2;   // code bytes of a row's chunk
                     mbar_expect_tx(&full[s], S::kMats * kTile * kCodeRow + bbytes);
                     tma_load_2d(stg, &tm_a0, c * kCodeRow, row, &full[s]);
-                    if (kPair) tma_load_2d(stg + kCodeBytes, &tm_a1, c * kCodeRow, row, &full[s]);
+                    if (kPair) tma_load_2d(stg + kCodeBytes, &tm_a1, c * kCodeRow, row + p.a1_row, &full[s]);
                     tma_load_2d(stg + S::kMats * kCodeBytes, tb, c * kKc, off, &full[s]);
                 }
             }
@@ -499,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, gbase += NC) {
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
             const int e = p.union_ids[u];
-            const size_t row = (size_t)e * p.rows_per_expert + tile * kTile + r;
+            const size_t row = (size_t)e * p.rows_per_expert + tile * p.tile_rows + r;
             const int NG = p.k_dim / kGroup;
             bool ok = true;
             if (p.vec_scales) {
@@ -572,11 +579,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * kAccStride;
-            const int orow = tile * kTile + r;
+            const int orow = tile * p.tile_rows + r;
             for (int n0 = 0; n0 < m; n0 += 16) {
                 float v0[16];
                 tmem_ld16(tbase + n0, v0);
-                if (kPair) {
+                if (kHOut) {
                     float v1[16];
                     tmem_ld16(tbase + kUpCol + n0, v1);
                     const int pos = perm8(orow);
@@ -591,6 +598,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (n0 + j < m) p.oout[(size_t)(off + n0 + j) * p.out_ld + orow] = v0[j];
+                    if (kPair) {                       // the unit's second down tile, 128 rows on
+                        float v1[16];
+                        tmem_ld16(tbase + kUpCol + n0, v1);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (n0 + j < m) p.oout[(size_t)(off + n0 + j) * p.out_ld + orow + kTile] = v1[j];
+                    }
                 }
             }
             tc_fence_before();
@@ -672,7 +686,7 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kPair, bool kQ2>
+template <bool kPair, bool kQ2, bool kHOut>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap (&b)[4],
                       const TcParams &p, cudaStream_t s, int grid) {
     // More than half of an SM's shared memory: one CTA per SM.  Two resident
@@ -680,9 +694,9 @@ cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtens
     // tcgen05.alloc until the first exits.
     const size_t smem = std::max<size_t>(Smem<kPair>::kBytes + 1024, 120 * 1024);
     static SmemLimits limits;
-    const cudaError_t e = allow_dynamic_smem(k_prefill_tc<kPair, kQ2>, limits, (int)smem);
+    const cudaError_t e = allow_dynamic_smem(k_prefill_tc<kPair, kQ2, kHOut>, limits, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_prefill_tc<kPair, kQ2>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
+    return launch_kernel(k_prefill_tc<kPair, kQ2, kHOut>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
                          b[1], b[2], b[3], p);
 }
 
@@ -714,6 +728,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     gu.n_tiles = a.F / kTile;
     gu.n_chunks = a.D / kKc;
     gu.rows_per_expert = a.F;
+    gu.tile_rows = kTile;
+    gu.a1_row = 0;
     gu.k_dim = a.D;
     gu.out_ld = a.F;
     gu.n_union = a.n_union;
@@ -724,20 +740,34 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     gu.vec_scales = (a.D / kGroup) % 8 == 0 && a16(a.gs) && a16(a.gb) && a16(a.us) && a16(a.ub);
     gu.hout = a.hbuf;
     gu.status = a.status;
-    if ((e = a.q2 ? launch_tc<true, true>(mg, mu, mx, gu, s, grid) : launch_tc<true, false>(mg, mu, mx, gu, s, grid)) !=
+    if ((e = a.q2 ? launch_tc<true, true, true>(mg, mu, mx, gu, s, grid) : launch_tc<true, false, true>(mg, mu, mx, gu, s, grid)) !=
         cudaSuccess)
         return e;
     TcParams dn = gu;
     dn.n_tiles = a.D / kTile;
     dn.n_chunks = a.F / kKc;
     dn.rows_per_expert = a.D;
+    dn.tile_rows = kTile;
+    dn.a1_row = 0;
     dn.k_dim = a.F;
     dn.out_ld = a.D;
     dn.s0 = a.ds; dn.b0 = a.db; dn.s1 = nullptr; dn.b1 = nullptr;
     dn.vec_scales = (a.F / kGroup) % 8 == 0 && a16(a.ds) && a16(a.db);
     dn.hout = nullptr;
     dn.oout = a.obuf;
-    return a.q2 ? launch_tc<false, true>(md, md, mh, dn, s, grid) : launch_tc<false, false>(md, md, mh, dn, s, grid);
+    if ((a.D / kTile) % 2 == 0) {
+        // pairs of adjacent 128-row down tiles: each chunk's activation tile
+        // feeds both, as gate and up share theirs
+        const size_t tile_groups = (size_t)kTile * (a.F / kGroup);   // scale entries of 128 rows
+        dn.n_tiles = a.D / (2 * kTile);
+        dn.tile_rows = 2 * kTile;
+        dn.a1_row = kTile;
+        dn.s1 = a.ds + tile_groups;
+        dn.b1 = a.db + tile_groups;
+        dn.vec_scales = dn.vec_scales && a16(dn.s1) && a16(dn.b1);
+        return a.q2 ? launch_tc<true, true, false>(md, md, mh, dn, s, grid) : launch_tc<true, false, false>(md, md, mh, dn, s, grid);
+    }
+    return a.q2 ? launch_tc<false, true, false>(md, md, mh, dn, s, grid) : launch_tc<false, false, false>(md, md, mh, dn, s, grid);
 }
 
 }  // namespace smoe
