@@ -35,9 +35,12 @@
 // work is a few instructions: one lane per group, min/max on bf16 pairs, and
 // per two weights a few packed fp32 operations that round RN(w - mn) *
 // RN(1 / scale) to a candidate code and measure how far the product sits from
-// it.  Only a weight within 2^-17 of a midpoint between two levels (where the
-// candidate could differ from the exact answer) takes a branch that decides
-// its code exactly.
+// it.  A weight within 2^-17 of a midpoint between two levels (where the
+// candidate could differ from the exact answer) is decided exactly later: its
+// byte of the code block goes into a per-warp queue, and whenever 16 or more
+// are queued the warp decides up to 32 of them at once, one per lane, and
+// overwrites those bytes -- the few such weights cost a share of one warp pass
+// instead of a pass of their own for every warp they occur in.
 #include "common.cuh"
 #include "dense.h"
 #include "kernels.h"
@@ -209,28 +212,34 @@ __device__ __forceinline__ int cmp_exact(float dh, float dl, float c) {
     return dl > 0.f ? 1 : (dl < 0.f ? -1 : 0);
 }
 
-// Code bits (0x4B000000 + q) of one weight decided exactly: q is the integer
-// nearest to (wk - mnk) / sk, halves to even, given a candidate q0 (the bits
-// `cbits`) known to be within one of it.  wk - mnk is held as the binary32 sum
-// and its exact error (Knuth's TwoSum) and compared with the two midpoints
-// sk (q0 -+ 1/2), which are exact in binary32 (8 significant bits times at
-// most 6).
-__device__ __forceinline__ uint32_t exact_cbits(float wk, float mnk, float sk, uint32_t cbits) {
+// Code q of one weight, decided exactly: q0 is the
+// fast path's candidate and e = d r - q0 its residual; the exact quotient is
+// within 2^-19 of d r, so it can lie beyond the midpoint on e's side only, and
+// that one midpoint s (q0 +- 1/2) -- exact in binary32 -- is compared with the
+// exact difference w - mn (Knuth's TwoSum).  Halves go to the even level.
+__device__ __forceinline__ uint32_t exact_q1(float w, float kk, float mnk, float sk, float r) {
+    const float d = __fmaf_rn(w, kk, -mnk);
+    const uint32_t cbits = __float_as_uint(__fmaf_rn(d, r, 8388608.0f));
+    const int q0 = (int)(cbits - 0x4B000000u);
+    const float e = __fmaf_rn(d, r, -(float)q0);
+    const float wk = __fmul_rn(w, kk);
     const float dh = __fsub_rn(wk, mnk);
     const float bb = __fsub_rn(dh, wk);
     const float dl = __fadd_rn(__fsub_rn(wk, __fsub_rn(dh, bb)), __fsub_rn(-mnk, bb));
-    const int q0 = (int)(cbits - 0x4B000000u);
-    const int hi = cmp_exact(dh, dl, __fmul_rn(sk, (float)q0 + 0.5f));
-    const int lo = cmp_exact(dh, dl, __fmul_rn(sk, (float)q0 - 0.5f));
+    const bool up = e >= 0.f;
+    const int t = cmp_exact(dh, dl, __fmul_rn(sk, (float)q0 + (up ? 0.5f : -0.5f)));
     int q = q0;
-    if (hi > 0 || (hi == 0 && (q0 & 1))) q = q0 + 1;
-    else if (lo < 0 || (lo == 0 && (q0 & 1))) q = q0 - 1;
-    return 0x4B000000u + (uint32_t)q;
+    if (up) {
+        if (t > 0 || (t == 0 && (q0 & 1))) q = q0 + 1;
+    } else {
+        if (t < 0 || (t == 0 && (q0 & 1))) q = q0 - 1;
+    }
+    return (uint32_t)q;
 }
 
 // The codes of a group whose scale is above 2^120 (its reciprocal would be
 // near binary32's subnormal range, so no candidate is computed): every weight
-// is compared with every midpoint s (k + 1/2), exactly as in exact_cbits.
+// is compared with every midpoint s (k + 1/2), exactly as in exact_q1.
 // Such a group needs weights near 2^124 and never occurs in practice; it is
 // kept so that every finite input has its exact codes.  `row` is the lane's 64
 // weights as they sit in its swizzled shared-memory row.
@@ -272,17 +281,18 @@ __device__ __noinline__ void q_group_huge(const unsigned char *row, int lane, fl
 //   t  = RN(e e - (1/4 - 2^-17))        t >= 0 only near a midpoint
 // d r is within 2^-19 of the exact (w - mn) / s, so a weight with |e| below
 // 1/2 - 2^-17 has q0 as its one nearest level.  The sign of t of both weights
-// of each pair goes into a 32-bit mask; after the pass, each pair whose mask
-// bit is clear (an exact tie or a weight within 2^-17 of a midpoint: about one
-// pair in 250 for real weights) has its two codes re-decided exactly
-// (exact_cbits) and patched into its code word.  The n = 32 / kBits words e_k
-// of a code word combine into sum_k q_k 2^(kBits k) as
+// of each pair goes into a 32-bit mask (one funnel shift a pair), returned as
+// `flags`: a set bit marks a pair with an exact tie or a weight within 2^-17
+// of a midpoint (about one pair in 300 for the bf16 weights here), whose codes
+// the caller has decided exactly (exact_q1) after the words are stored.  The
+// n = 32 / kBits words e_k of a code word combine into sum_k q_k 2^(kBits k) as
 // (sum_k e_k 2^(kBits k)) minus 0x4B000000 * sum_k 2^(kBits k) (mod 2^32), one
 // shift-add each.  A group whose scale is above 2^120 is coded by
 // q_group_huge, which writes the codes itself (returns true).
 template <int kBits>
 __device__ __forceinline__ bool q_group(const unsigned char *row, int lane, uint32_t (&code)[2 * kBits],
-                                        uint16_t &sb, uint16_t &bb, uint32_t *out) {
+                                        uint16_t &sb, uint16_t &bb, uint32_t *out, uint32_t &flags) {
+    flags = 0u;
     constexpr int kWords = 2 * kBits, kPairs = 16 / kBits;  // code words; bf16 pairs per code word
     constexpr uint32_t kPackBias = kBits == 4 ? 0xFB000000u : 0xE7000000u;   // 0x4B000000 * 0x11111111 / 0x55555555
     constexpr float kLevels = (float)((1 << kBits) - 1);
@@ -341,31 +351,42 @@ __device__ __forceinline__ bool q_group(const unsigned char *row, int lane, uint
             const float2 c = ffma2(d, r2, m23);
             const float2 e = ffma2(d, r2, fsub2(m23, c));    // m23 - c = -q0 exactly
             const float2 t = ffma2(e, e, ntie);
-            clear = (clear << 1) + ((__float_as_uint(t.x) & __float_as_uint(t.y)) >> 31);
+            clear = __funnelshift_l(__float_as_uint(t.x) & __float_as_uint(t.y), clear, 1);
             acc = (acc << kBits) + __float_as_uint(c.y);
             acc = (acc << kBits) + __float_as_uint(c.x);
         }
         code[k] = acc - kPackBias;
     }
-    // the pairs near a midpoint, decided exactly
-    for (uint32_t fl = ~clear; fl != 0;) {
-        const int n = __clz(fl);
-        fl &= ~(0x80000000u >> n);
-        const int k = n / kPairs, j = kPairs - 1 - n % kPairs, pi = kPairs * k + j;   // pair: elements 2pi, 2pi+1
-        const uint32_t p = *reinterpret_cast<const uint32_t *>(row + (((pi >> 2) ^ lane) & 7) * 16 + (pi & 3) * 4);
-        const float wx = __uint_as_float(p << 16), wy = __uint_as_float(p & 0xFFFF0000u);
-        const uint32_t cx = exact_cbits(__fmul_rn(wx, kk), mnk, sk,
-                                        __float_as_uint(__fmaf_rn(__fmaf_rn(wx, kk, -mnk), r, 8388608.0f)));
-        const uint32_t cy = exact_cbits(__fmul_rn(wy, kk), mnk, sk,
-                                        __float_as_uint(__fmaf_rn(__fmaf_rn(wy, kk, -mnk), r, 8388608.0f)));
-        const int sh = 2 * kBits * j;
-        const uint32_t field = ((cx - 0x4B000000u) | ((cy - 0x4B000000u) << kBits)) << sh;
-        const uint32_t msk = ((1u << (2 * kBits)) - 1u) << sh;
-#pragma unroll
-        for (int w = 0; w < kWords; ++w)
-            if (w == k) code[w] = (code[w] & ~msk) | field;
-    }
+    flags = ~clear;                 // pairs near a midpoint (bit 31 - n: pair n in processing order)
     return false;
+}
+
+// A byte of a group's code block whose codes the fast pass could not decide:
+// its weights (SMOE-Q4: the pair of the byte; SMOE-Q2: its four weights), the
+// group's bf16 scale and minimum, and the byte's index in the code array.
+struct FixItem {
+    uint2 w;            // bf16 weights, lowest element first
+    uint32_t sb_bb;     // scale | minimum << 16 (bf16)
+    uint32_t at_lo, at_hi;
+};
+constexpr int kFixCap = 48;             // queue entries per warp (at most 15 + 32 at a time)
+
+// Decides one queued byte exactly (the scalings as in q_group) and stores it.
+template <int kBits>
+__device__ __forceinline__ void fix_item(const FixItem &it, uint8_t *codes) {
+    const float s = bf16_to_f32((uint16_t)(it.sb_bb & 0xFFFFu)), mn = bf16_to_f32((uint16_t)(it.sb_bb >> 16));
+    const float kk = s < 0x1p-62f ? 0x1p64f : 1.0f;
+    const float sk = __fmul_rn(s, kk), mnk = __fmul_rn(mn, kk);
+    const float r = __frcp_rn(sk);
+    uint32_t byte = 0;
+    constexpr int kPer = 8 / kBits;     // weights of a byte
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const uint32_t word = i < 2 ? it.w.x : it.w.y;
+        const float wi = (i & 1) ? __uint_as_float(word & 0xFFFF0000u) : __uint_as_float(word << 16);
+        byte |= exact_q1(wi, kk, mnk, sk, r) << (kBits * i);
+    }
+    codes[((unsigned long long)it.at_hi << 32) | it.at_lo] = (uint8_t)byte;
 }
 
 // Warp steps of 32 groups (4 KiB) are handed out grid-stride; lane l
@@ -379,6 +400,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     k_quantize(const uint16_t *__restrict__ w, long long n_groups, uint8_t *__restrict__ codes,
                uint16_t *__restrict__ scale, uint16_t *__restrict__ bias) {
     __shared__ __align__(16) unsigned char ring[kQWarps][kQStages][4096];
+    __shared__ FixItem fq[kQWarps][kFixCap];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long warps = (long long)gridDim.x * kQWarps;
     const long long steps = (n_groups + 31) / 32;
@@ -398,6 +420,18 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     };
 #pragma unroll
     for (int i = 0; i < kQStages - 1; ++i) issue(i);
+    int qn = 0;                                              // queued items (warp-uniform)
+    // The first n (<= 32) queued items, one per lane, then the rest moved down.
+    auto flush = [&](int n) {
+        if (lane < n) fix_item<kBits>(fq[warp][lane], codes);
+        FixItem keep{};
+        const bool mv = n + lane < qn;
+        if (mv) keep = fq[warp][n + lane];
+        __syncwarp();
+        if (mv) fq[warp][lane] = keep;
+        qn -= n;
+        __syncwarp();
+    };
     for (long long i = 0; st0 + i * warps < steps; ++i) {
         issue(i + kQStages - 1);
         cp_async_wait<kQStages - 1>();                       // this lane's copies of step i landed
@@ -407,8 +441,9 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         const bool live = grp < n_groups;
         uint32_t code[2 * kBits];
         uint16_t sb, bb;
+        uint32_t flags;
         uint32_t *cq = reinterpret_cast<uint32_t *>(codes + (live ? grp : 0) * (8 * kBits));
-        const bool exact = q_group<kBits>(stage + lane * 128, lane, code, sb, bb, live ? cq : nullptr);
+        const bool exact = q_group<kBits>(stage + lane * 128, lane, code, sb, bb, live ? cq : nullptr, flags);
         if (live) {
             if (!exact) {
 #pragma unroll
@@ -418,8 +453,52 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             scale[grp] = sb;
             bias[grp] = bb;
         }
+        // Queue the bytes holding pairs near a midpoint; whenever 16 or more
+        // are queued, up to 32 are decided together, one per lane.  A byte
+        // written by another lane comes after the owning lane's word store
+        // above: the warp barriers between order them.
+        {
+            constexpr int kPairs = 16 / kBits;
+            uint32_t fl = (live && !exact) ? flags : 0u;
+            const unsigned char *row = stage + lane * 128;
+            while (__any_sync(0xffffffffu, fl != 0u)) {
+                int b = -1;
+                if (fl) {
+                    const int n = __clz(fl);
+                    const int k = n / kPairs, j = kPairs - 1 - n % kPairs, pi = kPairs * k + j;
+                    if (kBits == 4) {
+                        b = pi;
+                        fl &= ~(0x80000000u >> n);
+                    } else {
+                        b = pi >> 1;                                   // pairs 2b, 2b + 1 (same word)
+                        const int n0 = kPairs * k + kPairs - 1 - (2 * b - kPairs * k);
+                        fl &= ~((0x80000000u >> n0) | (0x80000000u >> (n0 - 1)));
+                    }
+                }
+                const uint32_t m = __ballot_sync(0xffffffffu, b >= 0);
+                if (b >= 0) {
+                    FixItem it;
+                    const int e0 = (8 / kBits) * b;                  // first element of the byte
+                    auto wpair = [&](int el) {                       // elements el, el + 1 (el even)
+                        const int c = el >> 3;
+                        return *reinterpret_cast<const uint32_t *>(row + ((c ^ lane) & 7) * 16 + (el & 7) * 2);
+                    };
+                    it.w.x = wpair(e0);
+                    it.w.y = kBits == 2 ? wpair(e0 + 2) : 0u;
+                    it.sb_bb = (uint32_t)sb | ((uint32_t)bb << 16);
+                    const unsigned long long at = (unsigned long long)grp * (8 * kBits) + (unsigned long long)b;
+                    it.at_lo = (uint32_t)at;
+                    it.at_hi = (uint32_t)(at >> 32);
+                    fq[warp][qn + __popc(m & ((1u << lane) - 1u))] = it;
+                }
+                qn += __popc(m);
+                __syncwarp();
+                if (qn >= 16) flush(qn < 32 ? qn : 32);          // leaves at most 15 queued
+            }
+        }
         __syncwarp();                                        // stage read by every lane: free to be refilled
     }
+    if (qn > 0) flush(qn);
     cp_async_wait<0>();
 }
 
