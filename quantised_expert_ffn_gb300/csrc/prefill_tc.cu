@@ -27,10 +27,12 @@
 //   warps 13-14 MMA: one thread of each issues tcgen05.mma with A from tensor
 //               memory (M=128 weight rows, K=16) and B from shared memory (N =
 //               pad16(bucket) tokens), fp16 x fp16 -> fp32 in TMEM, and commits
-//               stages back -- warp 13 the gate (or down) matrix, warp 14 the up
-//               matrix.  A thread blocks on each tcgen05.mma until the tensor
-//               pipe takes it; two issuing threads keep the pipe fed while
-//               either one waits on a barrier or commits;
+//               stages back -- warp 13 the first tile of the unit, warp 14 the
+//               second.  A thread blocks on each tcgen05.mma until the tensor
+//               pipe takes it, and its later shared-memory accesses (barrier
+//               waits included) queue behind the MMAs it issued, so each MMA
+//               thread waits only for the chunk's A: the dequant warps waited
+//               for the stage's tile before they released it;
 //   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
@@ -69,11 +71,16 @@ constexpr int kMma2Warp = 14;      // gate/up: the up matrix's MMA thread
 constexpr int kTile = 128;
 constexpr int kKc = 64;
 constexpr int kNmax = 64;
-// One ring of kStages stages: shared memory holds a stage's codes and
-// activation tile, TMEM columns from kACol0 its dequantised A.  A stage is
-// refilled only after the MMA that read it has completed (the TMA waits for
-// it), so a producer that sees the stage's codes land may overwrite its A.
-constexpr int kStages = 4;
+// Two rings.  kStages shared-memory stages hold a chunk's codes and
+// activation tile; a stage is refilled once its codes are read and the MMAs
+// that read its tile have completed (the TMA waits on its empty barrier).
+// kAStages TMEM stages (columns from kACol0) hold a chunk's dequantised A;
+// chunk g's A overwrites chunk g - kAStages's once that chunk's MMAs have
+// completed, i.e. once that chunk's shared-memory stage is empty -- the
+// producers wait on that phase, so the TMEM ring needs no barriers of its own
+// and the MMA threads one commit per chunk.
+constexpr int kStages = 8;
+constexpr int kAStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 128;                  // two accumulator buffers: columns 0-127, 128-255
 constexpr uint32_t kUpCol = 64;                       // up accumulator after gate's (N <= 64 columns each)
@@ -313,8 +320,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
     uint64_t *full = bars;                    // [kStages] codes + activations landed
     uint64_t *empty = full + kStages;         // [kStages] codes read and the stage's MMAs complete
-    uint64_t *afull = empty + kStages;        // [kStages] dequantised A written
-    uint64_t *accfull = afull + kStages;      // [2]
+    uint64_t *afull = empty + kStages;        // [kAStages] dequantised A written
+    uint64_t *accfull = afull + kAStages;     // [2]
     uint64_t *accempty = accfull + 2;         // [2]
     uint64_t *drain = accempty + 2;           // [2] all MMAs issued by MMA thread i complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kProdThreads / 2 + kIssuers);
         }
-        for (int i = 0; i < kStages; ++i) mbar_init(&afull[i], kProdThreads / 2);
+        for (int i = 0; i < kAStages; ++i) mbar_init(&afull[i], kProdThreads / 2);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accfull[i], kIssuers);
             mbar_init(&accempty[i], 128);
@@ -404,9 +411,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t d0 = tmem + b * kAccStride;
                 bool ok = true;
                 for (int c = 0; c < NC; ++c, ++g) {
-                    const int s = g % kStages, a = s;
-                    if (!mbar_wait(&afull[a], (g / kStages) & 1, abort_flag, p.status) ||
-                        !mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)) {
+                    const int s = g % kStages, a = g % kAStages;
+                    // the stage's tile has landed: the dequant warps waited for it
+                    // before releasing the chunk's A (afull orders this thread after them)
+                    if (!mbar_wait(&afull[a], (g / kAStages) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -442,7 +450,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // and store them into the stage's A columns.  false when a wait gave up.
         auto chunk = [&](int c, float s0f, float b0f, float s1f, float b1f) -> bool {
             const uint32_t g = gbase + (uint32_t)c;
-            const int s = g % kStages, a = s;
+            const int s = g % kStages, a = g % kAStages;
             if (!levels_in_fp16(s0f, b0f, kLv) || !levels_in_fp16(s1f, b1f, kLv))
                 set_status(p.status, SMOE_ERR_RANGE);
             const __half2 s0 = f2h2(s0f), b0 = f2h2(b0f), s1 = f2h2(s1f), b1 = f2h2(b1f);
@@ -494,7 +502,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dequant_word(c1b.w, s1, b1, q1[7]);
                 }
             }
-            tc_fence_after();      // A stage a: its last MMAs completed before these codes landed
+            // A stage a is free once the MMAs of chunk g - kAStages completed: that
+            // chunk's stage's empty phase (it cannot have moved on since: chunk
+            // g + kAStages is dequantised after this one)
+            if (g >= (uint32_t)kAStages) {
+                const uint32_t gp = g - kAStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[gp % kStages], (gp / kStages) & 1, abort_flag, p.status)))
+                    return false;
+            }
+            tc_fence_after();
             const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols;
             tmem_st32(acol, q0);
             if (kPair) tmem_st32(acol + kACols, q1);
