@@ -183,6 +183,47 @@ def test_quantize_adversarial_groups_bit_exact(smoe, orc, code_bits):
     assert np.array_equal(host(codes), c_ref)
 
 
+def all_tie_groups(n_groups, levels, seed):
+    """bf16 weights [n_groups, 64] of which 62 per group sit exactly on a
+    midpoint mn + s (k + 1/2) between two of the `levels` + 1 levels, the other
+    two being the group's least and greatest weight (mn and mn + levels * s).
+    s = c * 2^e with c odd and below 8, so the quantiser's scale
+    bf16((mx - mn) / levels) is s itself and every quotient is an exact
+    half; each such code is decided by the halves-to-even rule alone."""
+    g = np.random.default_rng(seed)
+    out = np.zeros((n_groups, 64), dtype=np.float64)
+    for i in range(n_groups):
+        e = int(g.integers(-30, 10))
+        s = int(g.choice([1, 3, 5, 7])) * 2.0 ** e
+        mn = -int(g.integers(0, 64)) * 2.0 ** (e - 1)
+        v = mn + s * (g.integers(0, levels, 64) + 0.5)
+        v[0], v[1] = mn, mn + levels * s
+        out[i] = g.permutation(v)
+    w = torch.from_numpy(out.astype(np.float32)).to(torch.bfloat16)
+    assert np.array_equal(w.double().numpy(), out)            # every value exact in bf16
+    return bits(w)
+
+
+@pytest.mark.parametrize("code_bits", [4, 2])
+@pytest.mark.parametrize("rows,cols", [(37, 576), (1024, 512)])
+def test_quantize_all_tie_groups_bit_exact(smoe, orc, code_bits, rows, cols):
+    """Every group of every warp step holds 62 exact ties, so every lane queues
+    the most bytes a group can need re-deciding and the queue flushes many
+    times within each step; 333 groups leave a partial last step.  Codes,
+    scales and biases equal the oracle's."""
+    levels = 15 if code_bits == 4 else 3
+    Wb = all_tie_groups(rows * cols // 64, levels, seed=rows + code_bits).reshape(rows, cols)
+    W = from_bits(Wb).cuda()
+    codes = torch.empty((rows, cols * code_bits // 8), dtype=torch.uint8, device="cuda")
+    scale = torch.empty((rows, cols // 64), dtype=torch.bfloat16, device="cuda")
+    bias = torch.empty_like(scale)
+    (smoe.smoe_quantize_q4 if code_bits == 4 else smoe.smoe_quantize_q2)(W, codes, scale, bias)
+    torch.cuda.synchronize()
+    c_ref, s_ref, b_ref = (orc.quantize_q4 if code_bits == 4 else orc.quantize_q2)(Wb)
+    assert np.array_equal(host(scale), s_ref) and np.array_equal(host(bias), b_ref)
+    assert np.array_equal(host(codes), c_ref)
+
+
 def test_quantize_q4_full_layer_tensor(smoe, orc):
     """A 30B layer's gate tensor (128 x 768 x 2048 bf16, 402 MB), as the
     benchmark runs it: 64 sampled rows bit-exact against the oracle, and the
