@@ -251,15 +251,27 @@ __device__ __forceinline__ bool levels_in_fp16(float s, float b, float L) {
     return fabsf(b) <= 65504.f && fabsf(fmaf(s, L, b)) <= 65504.f;
 }
 
+__device__ __forceinline__ uint32_t or_masked(uint32_t a, uint32_t mask, uint32_t c) {   // (a & mask) | c
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
+    return d;
+}
+
 // 8 codes of one word -> 4 half2 (e_i, e_{i+4}), each s*q + b with one rounding.
+// A code in bits 0-3 of a half-word under the exponent of 1024 (0x6400) is the
+// fp16 1024 + q; one in bits 4-7 under the exponent of 64 (0x5400) is 64 + q
+// (the mantissa's unit there is 1/16); a subtraction leaves q exactly.  So the
+// lower byte pair needs no shift and the upper one a single shift by 8.
 __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
     const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    const __half2 k64 = __halves2half2(__ushort_as_half(0x5400), __ushort_as_half(0x5400));
+    const uint32_t w8 = w >> 8;
+    const uint32_t m[4] = {or_masked(w, 0x000F000Fu, 0x64006400u), or_masked(w, 0x00F000F0u, 0x54005400u),
+                           or_masked(w8, 0x000F000Fu, 0x64006400u), or_masked(w8, 0x00F000F0u, 0x54005400u)};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        uint32_t m;
-        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(m) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x64006400u));
-        __half2 q = __hsub2(*reinterpret_cast<__half2 *>(&m), k1024);   // exact q
-        __half2 v = __hfma2(q, s2, b2);                                   // s*q + b, one rounding
+        const __half2 q = __hsub2(*reinterpret_cast<const __half2 *>(&m[i]), (i & 1) ? k64 : k1024);  // exact q
+        __half2 v = __hfma2(q, s2, b2);                                                            // s*q + b, one rounding
         o[i] = *reinterpret_cast<uint32_t *>(&v);
     }
 }
@@ -459,6 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 return false;
             const unsigned char *stg = st_ring + s * S::kStageBytes;
             uint32_t q0[8][4], q1[8][4];
+            uint4 c1a{}, c1b{};                       // SMOE-Q4: the second matrix's codes
             if constexpr (kQ2) {                      // 16 bytes per row
                 const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 16);
                 uint4 c1 = c0;
@@ -477,7 +490,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {                                  // 32 bytes per row
                 const uint4 c0a = *reinterpret_cast<const uint4 *>(stg + r * 32);
                 const uint4 c0b = *reinterpret_cast<const uint4 *>(stg + r * 32 + 16);
-                uint4 c1a = c0a, c1b = c0b;
                 if (kPair) {
                     c1a = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32);
                     c1b = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + 16);
@@ -491,16 +503,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 dequant_word(c0b.y, s0, b0, q0[5]);
                 dequant_word(c0b.z, s0, b0, q0[6]);
                 dequant_word(c0b.w, s0, b0, q0[7]);
-                if (kPair) {
-                    dequant_word(c1a.x, s1, b1, q1[0]);
-                    dequant_word(c1a.y, s1, b1, q1[1]);
-                    dequant_word(c1a.z, s1, b1, q1[2]);
-                    dequant_word(c1a.w, s1, b1, q1[3]);
-                    dequant_word(c1b.x, s1, b1, q1[4]);
-                    dequant_word(c1b.y, s1, b1, q1[5]);
-                    dequant_word(c1b.z, s1, b1, q1[6]);
-                    dequant_word(c1b.w, s1, b1, q1[7]);
-                }
             }
             // A stage a is free once the MMAs of chunk g - kAStages completed: that
             // chunk's stage's empty phase (it cannot have moved on since: chunk
@@ -513,6 +515,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols;
             tmem_st32(acol, q0);
+            if constexpr (!kQ2) {
+                // the second matrix is converted once the first is on its way to
+                // tensor memory: half the converted values live at a time
+                if (kPair) {
+                    dequant_word(c1a.x, s1, b1, q1[0]);
+                    dequant_word(c1a.y, s1, b1, q1[1]);
+                    dequant_word(c1a.z, s1, b1, q1[2]);
+                    dequant_word(c1a.w, s1, b1, q1[3]);
+                    dequant_word(c1b.x, s1, b1, q1[4]);
+                    dequant_word(c1b.y, s1, b1, q1[5]);
+                    dequant_word(c1b.z, s1, b1, q1[6]);
+                    dequant_word(c1b.w, s1, b1, q1[7]);
+                }
+            }
             if (kPair) tmem_st32(acol + kACols, q1);
             tmem_wait_st();
             tc_fence_before();
