@@ -12,18 +12,21 @@
 //
 // One persistent CTA per SM walks a static list of units (union expert u and
 // its row tiles: a 128-row tile of both gate and up, or two adjacent 128-row
-// tiles of down, so that every chunk of a unit feeds two MMA threads from one
-// activation tile); per unit the K dimension is consumed in chunks of 64 (one
-// Q4 group).  Warp roles:
-//   warps 0-7   dequant: read the TMA-staged codes of a chunk from shared
+// tiles of down, so that every stage of a unit feeds two MMA threads from one
+// set of activation tiles); per unit the K dimension is consumed in stages of
+// two Q4 groups (128 codes: a 64-byte slice of each Q4 row, which the memory
+// system serves faster than 32-byte slices).  Warp roles:
+//   warps 0-7   dequant: read the TMA-staged codes of a stage from shared
 //               memory, turn them into fp16 w = s*q + b (one rounding; exact
-//               when b = -8 s, since s*(q-8) needs at most 11 bits) and store
-//               them straight into tensor memory (tcgen05.st): warp w owns
-//               TMEM lanes 32*(w%4).. = tile rows, and the chunks of parity
-//               w/4, so the two dequant warps of a scheduler work on alternate
-//               chunks and one's waits overlap the other's arithmetic;
-//   warp 12     TMA: codes tiles (no swizzle) and the bucket's activation
-//               tile (128-byte swizzle) into a ring of shared-memory stages;
+//               when b = -8 s, since s*(q-8) needs at most 11 bits) group by
+//               group and store them straight into tensor memory
+//               (tcgen05.st): warp w owns TMEM lanes 32*(w%4).. = tile rows,
+//               and the stages of parity w/4, so the two dequant warps of a
+//               scheduler work on alternate stages and one's waits overlap the
+//               other's arithmetic;
+//   warp 12     TMA: code tiles (no swizzle) and the bucket's activation
+//               tiles (128-byte swizzle, one per group) into a ring of
+//               shared-memory stages;
 //   warps 13-14 MMA: one thread of each issues tcgen05.mma with A from tensor
 //               memory (M=128 weight rows, K=16) and B from shared memory (N =
 //               pad16(bucket) tokens), fp16 x fp16 -> fp32 in TMEM, and commits
@@ -31,8 +34,8 @@
 //               second.  A thread blocks on each tcgen05.mma until the tensor
 //               pipe takes it, and its later shared-memory accesses (barrier
 //               waits included) queue behind the MMAs it issued, so each MMA
-//               thread waits only for the chunk's A: the dequant warps waited
-//               for the stage's tile before they released it;
+//               thread waits only for the stage's A: the dequant warps waited
+//               for the stage's tiles before they released it;
 //   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
@@ -71,22 +74,28 @@ constexpr int kMma2Warp = 14;      // gate/up: the up matrix's MMA thread
 constexpr int kTile = 128;
 constexpr int kKc = 64;
 constexpr int kNmax = 64;
-// Two rings.  kStages shared-memory stages hold a chunk's codes and
-// activation tile; a stage is refilled once its codes are read and the MMAs
-// that read its tile have completed (the TMA waits on its empty barrier).
-// kAStages TMEM stages (columns from kACol0) hold a chunk's dequantised A;
-// chunk g's A overwrites chunk g - kAStages's once that chunk's MMAs have
-// completed, i.e. once that chunk's shared-memory stage is empty -- the
-// producers wait on that phase, so the TMEM ring needs no barriers of its own
-// and the MMA threads one commit per chunk.
-constexpr int kStages = 8;
-constexpr int kAStages = 4;
+// Two rings.  kStages shared-memory stages hold kGpc groups' codes and
+// activation tiles; a stage is refilled once its codes are read and the MMAs
+// that read its tiles have completed (the TMA waits on its empty barrier).
+// kAStages TMEM stages (columns from kACol0) hold a stage's dequantised A;
+// stage g's A overwrites stage g - kAStages's once that stage's MMAs have
+// completed, i.e. once its shared-memory stage is empty -- the producers wait
+// on that phase, so the TMEM ring needs no barriers of its own and the MMA
+// threads one commit per stage.  (The dequant warps release a stage's codes
+// only through that same barrier, after the MMAs: a TMA write may not follow
+// their reads of the same bytes without a proxy fence, and by then the values
+// read have long been consumed.)  Ring depths of 4 to 7 stages measure within
+// 3 % of each other.
+constexpr int kGpc = 2;      // Q4 groups (64-code chunks along K) per stage
+constexpr int kStages = 6;
+constexpr int kAStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 128;                  // two accumulator buffers: columns 0-127, 128-255
 constexpr uint32_t kUpCol = 64;                       // up accumulator after gate's (N <= 64 columns each)
 constexpr uint32_t kACol0 = 256;                      // A stages: columns 256-511
 constexpr uint32_t kACols = 32;                       // one matrix's 128 x 64 fp16 chunk: 32 columns
-constexpr int kCodeBytes = kTile * kKc / 2;          // 4 KB of codes per matrix per stage
+constexpr uint32_t kAMatCols = kGpc * kACols;         // one matrix's columns of a stage
+constexpr int kCodeBytes = kTile * kKc * kGpc / 2;   // 8 KB of codes per matrix per stage
 constexpr int kBTileBytes = kNmax * kKc * 2;         // 8 KB fp16 B tile (up to 64 rows)
 
 struct TcParams {
@@ -308,13 +317,13 @@ __device__ __forceinline__ int perm8(int f) {   // position of element f in the 
 template <bool kPair>
 struct Smem {
     static constexpr int kMats = kPair ? 2 : 1;
-    static constexpr int kStageBytes = kMats * kCodeBytes + kBTileBytes;
+    static constexpr int kStageBytes = kMats * kCodeBytes + kGpc * kBTileBytes;
     static constexpr int kStageOff = 0;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
     static constexpr int kBytes = kBarOff + 1024;   // barriers + tmem slot + flags
 };
 
-// kPair: two 128-row A tiles per unit share each chunk's activation tile --
+// kPair: two 128-row A tiles per unit share each stage's activation tiles --
 // gate and up (kHOut: the epilogue writes h = SiLU(g) * u), or two adjacent
 // tiles of the down matrix (the epilogue writes both as fp32 outputs).
 template <bool kPair, bool kQ2, bool kHOut>
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // A chunk is dequantised by the 4 warps of its parity (128 threads) and
+    // A stage is dequantised by the 4 warps of its parity (128 threads) and
     // multiplied by one MMA thread per matrix, each committing on its own.
     constexpr uint32_t kIssuers = kPair ? 2 : 1;
     if (tid == 0) {
@@ -376,6 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nu = *p.n_union;
     const int n_units = nu * p.n_tiles;
     const int NC = p.n_chunks;
+    const int NSC = NC / kGpc;       // stages per unit (K is a multiple of 128)
 
     if (warp == kTmaWarp) {
         if (lane == 0) {
@@ -390,16 +400,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const CUtensorMap *tb = nb <= 1 ? &tm_b16 : nb == 2 ? &tm_b32 : nb == 3 ? &tm_b48 : &tm_b64;
                 const uint32_t bbytes = (uint32_t)(nb < 1 ? 1 : nb) * 16 * kKc * 2;  // full box, OOB rows zero-filled
                 const int row = e * p.rows_per_expert + tile * p.tile_rows;
-                for (int c = 0; c < NC; ++c, ++g) {
+                for (int c = 0; c < NSC; ++c, ++g) {
                     const int s = g % kStages;
                     const uint32_t ph = (g / kStages) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
                     unsigned char *stg = st_ring + s * S::kStageBytes;
-                    constexpr int kCodeRow = kQ2 ? kKc / 4 : kKc / 2;   // code bytes of a row's chunk
-                    mbar_expect_tx(&full[s], S::kMats * kTile * kCodeRow + bbytes);
+                    constexpr int kCodeRow = kGpc * (kQ2 ? kKc / 4 : kKc / 2);   // code bytes of a row's stage
+                    mbar_expect_tx(&full[s], S::kMats * kTile * kCodeRow + kGpc * bbytes);
                     tma_load_2d(stg, &tm_a0, c * kCodeRow, row, &full[s]);
                     if (kPair) tma_load_2d(stg + kCodeBytes, &tm_a1, c * kCodeRow, row + p.a1_row, &full[s]);
-                    tma_load_2d(stg + S::kMats * kCodeBytes, tb, c * kKc, off, &full[s]);
+#pragma unroll
+                    for (int h = 0; h < kGpc; ++h)
+                        tma_load_2d(stg + S::kMats * kCodeBytes + h * kBTileBytes, tb, (c * kGpc + h) * kKc, off, &full[s]);
                 }
             }
             // drain: every stage issued must have landed before the CTA exits
@@ -422,20 +434,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem + b * kAccStride;
                 bool ok = true;
-                for (int c = 0; c < NC; ++c, ++g) {
+                for (int c = 0; c < NSC; ++c, ++g) {
                     const int s = g % kStages, a = g % kAStages;
-                    // the stage's tile has landed: the dequant warps waited for it
-                    // before releasing the chunk's A (afull orders this thread after them)
+                    // the stage's tiles have landed: the dequant warps waited for them
+                    // before releasing the stage's A (afull orders this thread after them)
                     if (!mbar_wait(&afull[a], (g / kAStages) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issued = true;
-                    const uint32_t acol = tmem + kACol0 + a * S::kMats * kACols;
-                    const uint64_t bd = smem_desc_sw128(smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes));
-                    const uint32_t acc = c > 0 ? 1u : 0u;
-                    mma_chunk_ta(d0 + mat * kUpCol, acol + mat * kACols, bd, idesc, acc);
+                    const uint32_t acol = tmem + kACol0 + a * S::kMats * kAMatCols + mat * kAMatCols;
+                    const uint32_t bsm = smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes);
+#pragma unroll
+                    for (int h = 0; h < kGpc; ++h)
+                        mma_chunk_ta(d0 + mat * kUpCol, acol + h * kACols, smem_desc_sw128(bsm + h * kBTileBytes), idesc,
+                                     (c > 0 || h > 0) ? 1u : 0u);
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
@@ -450,102 +464,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp < 8) {
         // ---------------- dequant producers ----------------
         // warp w writes TMEM lanes 32*(w%4).. (its quarter of the tile's rows)
-        // for the chunks of parity w/4, the chunk's full 64 codes of each matrix;
-        // the two warps of a scheduler thus work on alternate chunks, and one's
+        // for the stages of parity w/4, the stage's kGpc groups of each matrix;
+        // the two warps of a scheduler thus work on alternate stages, and one's
         // waits overlap the other's arithmetic.
         const int rq = warp & 3, cp = warp >> 2;
         const int r = 32 * rq + lane;
         const uint32_t tlane = (uint32_t)(32 * rq) << 16;
         constexpr float kLv = kQ2 ? 3.f : 15.f;
-        uint32_t gbase = 0;     // global index of the current unit's chunk 0
-        // Chunk c of the unit: wait for its stage, turn the codes into fp16 s*q + b
-        // and store them into the stage's A columns.  false when a wait gave up.
-        auto chunk = [&](int c, float s0f, float b0f, float s1f, float b1f) -> bool {
+        uint32_t gbase = 0;     // global index of the current unit's stage 0
+        // Scales and biases of a stage's groups, matrix m, group h.
+        struct StageSB { float s[2][kGpc], b[2][kGpc]; };
+        // Stage c of the unit: wait for its tiles, turn the codes into fp16 s*q + b
+        // group by group and store them into the stage's A columns.  false when a
+        // wait gave up.
+        auto stage = [&](int c, const StageSB &sb) -> bool {
             const uint32_t g = gbase + (uint32_t)c;
             const int s = g % kStages, a = g % kAStages;
-            if (!levels_in_fp16(s0f, b0f, kLv) || !levels_in_fp16(s1f, b1f, kLv))
-                set_status(p.status, SMOE_ERR_RANGE);
-            const __half2 s0 = f2h2(s0f), b0 = f2h2(b0f), s1 = f2h2(s1f), b1 = f2h2(b1f);
-            // waits are warp-uniform: the TMEM store below is warp-collective
+            __half2 sh[2][kGpc], bh[2][kGpc];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int h = 0; h < kGpc; ++h) {
+                    if ((m == 0 || kPair) && !levels_in_fp16(sb.s[m][h], sb.b[m][h], kLv)) set_status(p.status, SMOE_ERR_RANGE);
+                    sh[m][h] = f2h2(sb.s[m][h]);
+                    bh[m][h] = f2h2(sb.b[m][h]);
+                }
+            // waits are warp-uniform: the TMEM stores below are warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.status)))
                 return false;
             const unsigned char *stg = st_ring + s * S::kStageBytes;
-            uint32_t q0[8][4], q1[8][4];
-            uint4 c1a{}, c1b{};                       // SMOE-Q4: the second matrix's codes
-            if constexpr (kQ2) {                      // 16 bytes per row
-                const uint4 c0 = *reinterpret_cast<const uint4 *>(stg + r * 16);
-                uint4 c1 = c0;
-                if (kPair) c1 = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 16);
-                mbar_arrive(&empty[s]);               // codes consumed
-                dequant_word_q2(c0.x, s0, b0, q0[0], q0[1]);
-                dequant_word_q2(c0.y, s0, b0, q0[2], q0[3]);
-                dequant_word_q2(c0.z, s0, b0, q0[4], q0[5]);
-                dequant_word_q2(c0.w, s0, b0, q0[6], q0[7]);
-                if (kPair) {
-                    dequant_word_q2(c1.x, s1, b1, q1[0], q1[1]);
-                    dequant_word_q2(c1.y, s1, b1, q1[2], q1[3]);
-                    dequant_word_q2(c1.z, s1, b1, q1[4], q1[5]);
-                    dequant_word_q2(c1.w, s1, b1, q1[6], q1[7]);
-                }
-            } else {                                  // 32 bytes per row
-                const uint4 c0a = *reinterpret_cast<const uint4 *>(stg + r * 32);
-                const uint4 c0b = *reinterpret_cast<const uint4 *>(stg + r * 32 + 16);
-                if (kPair) {
-                    c1a = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32);
-                    c1b = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + r * 32 + 16);
-                }
-                mbar_arrive(&empty[s]);               // codes consumed
-                dequant_word(c0a.x, s0, b0, q0[0]);
-                dequant_word(c0a.y, s0, b0, q0[1]);
-                dequant_word(c0a.z, s0, b0, q0[2]);
-                dequant_word(c0a.w, s0, b0, q0[3]);
-                dequant_word(c0b.x, s0, b0, q0[4]);
-                dequant_word(c0b.y, s0, b0, q0[5]);
-                dequant_word(c0b.z, s0, b0, q0[6]);
-                dequant_word(c0b.w, s0, b0, q0[7]);
-            }
-            // A stage a is free once the MMAs of chunk g - kAStages completed: that
-            // chunk's stage's empty phase (it cannot have moved on since: chunk
-            // g + kAStages is dequantised after this one)
-            if (g >= (uint32_t)kAStages) {
-                const uint32_t gp = g - kAStages;
-                if (!__all_sync(0xffffffffu, mbar_wait(&empty[gp % kStages], (gp / kStages) & 1, abort_flag, p.status)))
-                    return false;
-            }
-            tc_fence_after();
-            const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kACols;
-            tmem_st32(acol, q0);
-            if constexpr (!kQ2) {
-                // the second matrix is converted once the first is on its way to
-                // tensor memory: half the converted values live at a time
-                if (kPair) {
-                    dequant_word(c1a.x, s1, b1, q1[0]);
-                    dequant_word(c1a.y, s1, b1, q1[1]);
-                    dequant_word(c1a.z, s1, b1, q1[2]);
-                    dequant_word(c1a.w, s1, b1, q1[3]);
-                    dequant_word(c1b.x, s1, b1, q1[4]);
-                    dequant_word(c1b.y, s1, b1, q1[5]);
-                    dequant_word(c1b.z, s1, b1, q1[6]);
-                    dequant_word(c1b.w, s1, b1, q1[7]);
+            constexpr int kRowBytes = kGpc * (kQ2 ? 16 : 32);     // code bytes of a row's stage
+            constexpr int kVecs = kRowBytes / 16;
+            uint4 cw[2][kVecs];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int v = 0; v < kVecs; ++v)
+                    cw[m][v] = (m == 0 || kPair) ? *reinterpret_cast<const uint4 *>(stg + m * kCodeBytes + r * kRowBytes + 16 * v)
+                                                 : make_uint4(0, 0, 0, 0);
+            mbar_arrive(&empty[s]);                   // codes consumed
+            uint32_t q[8][4];
+            const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kAMatCols;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                if (m == 1 && !kPair) break;
+#pragma unroll
+                for (int h = 0; h < kGpc; ++h) {
+                    if constexpr (kQ2) {              // one 16-byte vector per group
+                        const uint4 w = cw[m][h];
+                        dequant_word_q2(w.x, sh[m][h], bh[m][h], q[0], q[1]);
+                        dequant_word_q2(w.y, sh[m][h], bh[m][h], q[2], q[3]);
+                        dequant_word_q2(w.z, sh[m][h], bh[m][h], q[4], q[5]);
+                        dequant_word_q2(w.w, sh[m][h], bh[m][h], q[6], q[7]);
+                    } else {                          // two per group
+                        const uint4 wa = cw[m][2 * h], wb = cw[m][2 * h + 1];
+                        dequant_word(wa.x, sh[m][h], bh[m][h], q[0]);
+                        dequant_word(wa.y, sh[m][h], bh[m][h], q[1]);
+                        dequant_word(wa.z, sh[m][h], bh[m][h], q[2]);
+                        dequant_word(wa.w, sh[m][h], bh[m][h], q[3]);
+                        dequant_word(wb.x, sh[m][h], bh[m][h], q[4]);
+                        dequant_word(wb.y, sh[m][h], bh[m][h], q[5]);
+                        dequant_word(wb.z, sh[m][h], bh[m][h], q[6]);
+                        dequant_word(wb.w, sh[m][h], bh[m][h], q[7]);
+                    }
+                    if (m == 0 && h == 0) {
+                        // A stage a is free once the MMAs of stage g - kAStages completed:
+                        // that stage's empty phase (it cannot have moved on since: stage
+                        // g + kAStages is dequantised after this one)
+                        if (g >= (uint32_t)kAStages) {
+                            const uint32_t gp = g - kAStages;
+                            if (!__all_sync(0xffffffffu, mbar_wait(&empty[gp % kStages], (gp / kStages) & 1, abort_flag, p.status)))
+                                return false;
+                        }
+                        tc_fence_after();
+                    }
+                    tmem_st32(acol + m * kAMatCols + h * kACols, q);
                 }
             }
-            if (kPair) tmem_st32(acol + kACols, q1);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&afull[a]);
             return true;
         };
-        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, gbase += NC) {
+        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, gbase += NSC) {
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
             const int e = p.union_ids[u];
             const size_t row = (size_t)e * p.rows_per_expert + tile * p.tile_rows + r;
             const int NG = p.k_dim / kGroup;
             bool ok = true;
             if (p.vec_scales) {
-                // Scales and biases of this row, 8 groups per 16-byte load, the
-                // next 8 requested one block ahead of use; of a block's 8 groups
-                // this warp takes those of its chunk parity (the cp-th bf16 of
-                // each 32-bit word).
+                // Scales and biases of this row, 8 groups (8 / kGpc stages) per 16-byte
+                // load, the next 8 requested one block ahead of use; of a block's
+                // stages this warp takes those of its parity.
                 uint4 vs0{}, vb0{}, vs1{}, vb1{}, ns0{}, nb0{}, ns1{}, nb1{};
                 auto load8 = [&](int c8, uint4 &ts0, uint4 &tb0, uint4 &ts1, uint4 &tb1) {
                     const size_t o = row * NG + c8;
@@ -556,10 +566,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tb1 = __ldg(reinterpret_cast<const uint4 *>(p.b1 + o));
                     }
                 };
-                const int sh = 16 * cp;
-                auto pick = [&](const uint4 &v, int j2) {
+                auto pick = [&](const uint4 &v, int gi) {      // group gi (0..7) of a block
+                    const int j2 = gi >> 1;
                     const uint32_t w = j2 == 0 ? v.x : j2 == 1 ? v.y : j2 == 2 ? v.z : v.w;
-                    return bf16_to_f32((uint16_t)(w >> sh));
+                    return bf16_to_f32((uint16_t)(w >> (16 * (gi & 1))));
                 };
                 load8(0, vs0, vb0, vs1, vb1);
                 if (NC > 8) load8(8, ns0, nb0, ns1, nb1);
@@ -569,22 +579,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (c8 + 8 < NC) load8(c8 + 8, ns0, nb0, ns1, nb1);
                     }
 #pragma unroll
-                    for (int j2 = 0; j2 < 4; ++j2) {
-                        const float s0f = pick(vs0, j2), b0f = pick(vb0, j2);
-                        const float s1f = kPair ? pick(vs1, j2) : s0f, b1f = kPair ? pick(vb1, j2) : b0f;
-                        if (!chunk(c8 + 2 * j2 + cp, s0f, b0f, s1f, b1f)) {
+                    for (int j = 0; j < 8 / kGpc / 2; ++j) {
+                        const int l = 2 * j + cp;                  // stage of the block
+                        StageSB sb;
+#pragma unroll
+                        for (int h = 0; h < kGpc; ++h) {
+                            sb.s[0][h] = pick(vs0, l * kGpc + h);
+                            sb.b[0][h] = pick(vb0, l * kGpc + h);
+                            sb.s[1][h] = kPair ? pick(vs1, l * kGpc + h) : sb.s[0][h];
+                            sb.b[1][h] = kPair ? pick(vb1, l * kGpc + h) : sb.b[0][h];
+                        }
+                        if (!stage(c8 / kGpc + l, sb)) {
                             ok = false;
                             break;
                         }
                     }
                 }
             } else {
-                for (int c = cp; c < NC; c += 2) {
-                    // scales/biases of this row and group (L1-cached: 16 groups share a sector)
-                    const float s0f = bf16_to_f32(p.s0[row * NG + c]), b0f = bf16_to_f32(p.b0[row * NG + c]);
-                    const float s1f = kPair ? bf16_to_f32(p.s1[row * NG + c]) : s0f;
-                    const float b1f = kPair ? bf16_to_f32(p.b1[row * NG + c]) : b0f;
-                    if (!chunk(c, s0f, b0f, s1f, b1f)) {
+                for (int c = cp; c < NSC; c += 2) {
+                    // scales/biases of this row's groups (L1-cached: 16 groups share a sector)
+                    StageSB sb;
+#pragma unroll
+                    for (int h = 0; h < kGpc; ++h) {
+                        const size_t o = row * NG + c * kGpc + h;
+                        sb.s[0][h] = bf16_to_f32(p.s0[o]);
+                        sb.b[0][h] = bf16_to_f32(p.b0[o]);
+                        sb.s[1][h] = kPair ? bf16_to_f32(p.s1[o]) : sb.s[0][h];
+                        sb.b[1][h] = kPair ? bf16_to_f32(p.b1[o]) : sb.b[0][h];
+                    }
+                    if (!stage(c, sb)) {
                         ok = false;
                         break;
                     }
@@ -741,11 +764,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap mg, mu, md, mx[4], mh[4];
     const int per_byte = a.q2 ? 4 : 2;                    // codes per byte
     bool ok = make_map(&mg, a.gq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / per_byte, (uint64_t)a.E * a.F,
-                       kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                       kGpc * kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               make_map(&mu, a.uq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.D / per_byte, (uint64_t)a.E * a.F,
-                       kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                       kGpc * kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               make_map(&md, a.dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.F / per_byte, (uint64_t)a.E * a.D,
-                       kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
+                       kGpc * kKc / per_byte, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
     for (int i = 0; i < 4 && ok; ++i)
         ok = make_map(&mx[i], a.xperm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.D, TK, kKc, 16 * (i + 1),
                       CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -788,7 +811,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     dn.hout = nullptr;
     dn.oout = a.obuf;
     if ((a.D / kTile) % 2 == 0) {
-        // pairs of adjacent 128-row down tiles: each chunk's activation tile
+        // pairs of adjacent 128-row down tiles: each stage's activation tiles
         // feeds both, as gate and up share theirs
         const size_t tile_groups = (size_t)kTile * (a.F / kGroup);   // scale entries of 128 rows
         dn.n_tiles = a.D / (2 * kTile);
