@@ -43,7 +43,10 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kRouteThreads) k_route_topk(RouteArgs a) {
+// At most 32 registers a thread, so 8 CTAs fit an SM and a 64-token chunk's
+// 1,024 CTAs run as one wave (at the 42 registers the code would otherwise
+// take, 5 per SM left a second wave).
+__global__ void __launch_bounds__(kRouteThreads, 8) k_route_topk(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int D = a.D, E = a.E, K = a.K;
     const int t = blockIdx.y;
