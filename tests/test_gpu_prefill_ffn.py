@@ -8,7 +8,9 @@ an error in the tensor-core FFN cannot hide behind the residual (which
 dominates y).  Cases: the 30B and 235B shapes, SMOE-Q4 and SMOE-Q2, chunks of
 1, 45 and 64 tokens (independent, or sharing a direction so the union holds
 ~60-100 experts), a Zipf(1.2)-skewed chunk, and a chunk whose tokens all
-route alike (every bucket full); then weights written by the library's own
+route alike (every bucket full), a ragged shape (6 and 10 groups: scales read
+group by group, an odd count of down tiles) and the largest layer taken;
+then weights written by the library's own
 quantiser (biases at the group minimum, not -8 s; some groups with scales
 below fp16's normal range) through decode and prefill; and the fp16 range
 bound of the tensor-core path."""
@@ -26,7 +28,12 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3      # fp32 expert outputs vs the oracle; bf16 residuals vs the oracle's bf16 y
 SIMT = os.environ.get("SMOE_PREFILL_PATH") == "simt"     # the CUDA-core engine (fp32, Q4 only)
 
-SHAPES = {"30b": (2048, 128, 8, 768), "235b": (4096, 128, 8, 1536)}
+# k384: D/64 = 6 and F/64 = 10 groups (scales read group by group, not 8 at a
+# time; 3 and 5 two-group stages) and an odd count of 128-row down tiles (one
+# tile per unit); max: the largest layer the library takes (d_model 8192,
+# 256 experts, top-16).
+SHAPES = {"30b": (2048, 128, 8, 768), "235b": (4096, 128, 8, 1536), "k384": (384, 32, 4, 640),
+          "max": (8192, 256, 16, 1024)}
 ALPHA = {"30b": 0.7, "235b": 0.6}
 
 
@@ -73,7 +80,8 @@ CASES = [("30b", 4, 1, "indep"), ("30b", 4, 45, "corr"), ("30b", 4, 64, "corr"),
          ("235b", 4, 1, "indep"), ("235b", 4, 45, "corr"), ("235b", 4, 64, "corr"),
          ("30b", 2, 1, "indep"), ("30b", 2, 64, "corr"), ("235b", 2, 45, "corr"),
          ("30b", 4, 64, "zipf"), ("30b", 2, 64, "zipf"),
-         ("30b", 4, 64, "one_bucket"), ("235b", 2, 64, "one_bucket")]
+         ("30b", 4, 64, "one_bucket"), ("235b", 2, 64, "one_bucket"),
+         ("k384", 4, 45, "indep"), ("k384", 2, 64, "indep"), ("max", 4, 8, "indep"), ("max", 2, 8, "indep")]
 
 
 @pytest.mark.parametrize("name,code_bits,T,kind", CASES)
