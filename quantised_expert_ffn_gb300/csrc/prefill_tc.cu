@@ -40,8 +40,10 @@
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
 // TMEM: columns 0-255 two accumulator buffers (gate, up: 64 columns each), so
-// the epilogue of one unit overlaps the main loop of the next; columns
-// 256-511 four stages of dequantised A.  Keeping A out of shared memory leaves
+// the epilogue of one unit overlaps the main loop of the next, and columns
+// 256-511 two stages of dequantised A (each two groups of both matrices); or,
+// for units of many stages (kOneAcc), one accumulator buffer in columns 0-127
+// and three A stages in 128-511.  Keeping A out of shared memory leaves
 // shared-memory bandwidth to the TMA and to the B operand.  Every wait on an
 // mbarrier is bounded: on timeout the CTA records SMOE_ERR_TIMEOUT, all roles
 // drain and the TMEM is freed.
@@ -88,11 +90,11 @@ constexpr int kNmax = 64;
 // 3 % of each other.
 constexpr int kGpc = 2;      // Q4 groups (64-code chunks along K) per stage
 constexpr int kStages = 6;
-constexpr int kAStages = 2;
+constexpr int kAStages = 2;   // with two accumulator buffers; 3 with one (kOneAcc)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 128;                  // two accumulator buffers: columns 0-127, 128-255
 constexpr uint32_t kUpCol = 64;                       // up accumulator after gate's (N <= 64 columns each)
-constexpr uint32_t kACol0 = 256;                      // A stages: columns 256-511
+constexpr uint32_t kACol0 = 256;                      // A stages: columns 256-511 (128-511 with one buffer)
 constexpr uint32_t kACols = 32;                       // one matrix's 128 x 64 fp16 chunk: 32 columns
 constexpr uint32_t kAMatCols = kGpc * kACols;         // one matrix's columns of a stage
 constexpr int kCodeBytes = kTile * kKc * kGpc / 2;   // 8 KB of codes per matrix per stage
@@ -326,7 +328,7 @@ struct Smem {
 // kPair: two 128-row A tiles per unit share each stage's activation tiles --
 // gate and up (kHOut: the epilogue writes h = SiLU(g) * u), or two adjacent
 // tiles of the down matrix (the epilogue writes both as fp32 outputs).
-template <bool kPair, bool kQ2, bool kHOut>
+template <bool kPair, bool kQ2, bool kHOut, bool kOneAcc>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
@@ -341,8 +343,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
     uint64_t *full = bars;                    // [kStages] codes + activations landed
     uint64_t *empty = full + kStages;         // [kStages] codes read and the stage's MMAs complete
-    uint64_t *afull = empty + kStages;        // [kAStages] dequantised A written
-    uint64_t *accfull = afull + kAStages;     // [2]
+    // kOneAcc: one accumulator buffer (columns 0-127) and three A stages, so
+    // that a stage's A waits for the MMAs of the stage three back, not two;
+    // the epilogue of a unit then no longer overlaps the next unit's MMAs
+    constexpr int kAS = kOneAcc ? 3 : kAStages;
+    constexpr uint32_t kAC0 = kOneAcc ? 128 : kACol0;
+    uint64_t *afull = empty + kStages;        // [kAS] dequantised A written
+    uint64_t *accfull = afull + 3;            // [2]
     uint64_t *accempty = accfull + 2;         // [2]
     uint64_t *drain = accempty + 2;           // [2] all MMAs issued by MMA thread i complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kProdThreads / 2 + kIssuers);
         }
-        for (int i = 0; i < kAStages; ++i) mbar_init(&afull[i], kProdThreads / 2);
+        for (int i = 0; i < kAS; ++i) mbar_init(&afull[i], kProdThreads / 2);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accfull[i], kIssuers);
             mbar_init(&accempty[i], 128);
@@ -429,22 +436,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 m = m > kNmax ? kNmax : m;
                 const int npad = ((m + 15) >> 4) << 4;
                 const uint32_t idesc = idesc_f16(kTile, npad < 16 ? 16 : npad);
-                const uint32_t b = i & 1;
-                if (!mbar_wait(&accempty[b], ((i >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+                const uint32_t b = kOneAcc ? 0u : (i & 1);
+                if (!mbar_wait(&accempty[b], (kOneAcc ? (i & 1) : ((i >> 1) & 1)) ^ 1, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem + b * kAccStride;
                 bool ok = true;
                 for (int c = 0; c < NSC; ++c, ++g) {
-                    const int s = g % kStages, a = g % kAStages;
+                    const int s = g % kStages, a = g % kAS;
                     // the stage's tiles have landed: the dequant warps waited for them
                     // before releasing the stage's A (afull orders this thread after them)
-                    if (!mbar_wait(&afull[a], (g / kAStages) & 1, abort_flag, p.status)) {
+                    if (!mbar_wait(&afull[a], (g / kAS) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issued = true;
-                    const uint32_t acol = tmem + kACol0 + a * S::kMats * kAMatCols + mat * kAMatCols;
+                    const uint32_t acol = tmem + kAC0 + a * S::kMats * kAMatCols + mat * kAMatCols;
                     const uint32_t bsm = smem_u32(st_ring + s * S::kStageBytes + S::kMats * kCodeBytes);
 #pragma unroll
                     for (int h = 0; h < kGpc; ++h)
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // wait gave up.
         auto stage = [&](int c, const StageSB &sb) -> bool {
             const uint32_t g = gbase + (uint32_t)c;
-            const int s = g % kStages, a = g % kAStages;
+            const int s = g % kStages, a = g % kAS;
             __half2 sh[2][kGpc], bh[2][kGpc];
 #pragma unroll
             for (int m = 0; m < 2; ++m)
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                  : make_uint4(0, 0, 0, 0);
             mbar_arrive(&empty[s]);                   // codes consumed
             uint32_t q[8][4];
-            const uint32_t acol = tmem + tlane + kACol0 + a * S::kMats * kAMatCols;
+            const uint32_t acol = tmem + tlane + kAC0 + a * S::kMats * kAMatCols;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 if (m == 1 && !kPair) break;
@@ -528,11 +535,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         dequant_word(wb.w, sh[m][h], bh[m][h], q[7]);
                     }
                     if (m == 0 && h == 0) {
-                        // A stage a is free once the MMAs of stage g - kAStages completed:
+                        // A stage a is free once the MMAs of stage g - kAS completed:
                         // that stage's empty phase (it cannot have moved on since: stage
-                        // g + kAStages is dequantised after this one)
-                        if (g >= (uint32_t)kAStages) {
-                            const uint32_t gp = g - kAStages;
+                        // g + kAS is dequantised after this one)
+                        if (g >= (uint32_t)kAS) {
+                            const uint32_t gp = g - kAS;
                             if (!__all_sync(0xffffffffu, mbar_wait(&empty[gp % kStages], (gp / kStages) & 1, abort_flag, p.status)))
                                 return false;
                         }
@@ -628,8 +635,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 set_status(p.status, SMOE_ERR_DEVICE);
                 m = kNmax;
             }
-            const uint32_t b = i & 1;
-            const bool got = mbar_wait(&accfull[b], (i >> 1) & 1, abort_flag, p.status);
+            const uint32_t b = kOneAcc ? 0u : (i & 1);
+            const bool got = mbar_wait(&accfull[b], kOneAcc ? (i & 1) : ((i >> 1) & 1), abort_flag, p.status);
             __syncwarp();                               // tcgen05.ld is warp-aligned
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
@@ -741,7 +748,7 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kPair, bool kQ2, bool kHOut>
+template <bool kPair, bool kQ2, bool kHOut, bool kOneAcc>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap (&b)[4],
                       const TcParams &p, cudaStream_t s, int grid) {
     // More than half of an SM's shared memory: one CTA per SM.  Two resident
@@ -749,9 +756,9 @@ cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtens
     // tcgen05.alloc until the first exits.
     const size_t smem = std::max<size_t>(Smem<kPair>::kBytes + 1024, 120 * 1024);
     static SmemLimits limits;
-    const cudaError_t e = allow_dynamic_smem(k_prefill_tc<kPair, kQ2, kHOut>, limits, (int)smem);
+    const cudaError_t e = allow_dynamic_smem(k_prefill_tc<kPair, kQ2, kHOut, kOneAcc>, limits, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_prefill_tc<kPair, kQ2, kHOut>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
+    return launch_kernel(k_prefill_tc<kPair, kQ2, kHOut, kOneAcc>, dim3(grid), dim3(kTcThreads), smem, s, true, a0, a1, b[0],
                          b[1], b[2], b[3], p);
 }
 
@@ -795,9 +802,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     gu.vec_scales = (a.D / kGroup) % 8 == 0 && a16(a.gs) && a16(a.gb) && a16(a.us) && a16(a.ub);
     gu.hout = a.hbuf;
     gu.status = a.status;
-    if ((e = a.q2 ? launch_tc<true, true, true>(mg, mu, mx, gu, s, grid) : launch_tc<true, false, true>(mg, mu, mx, gu, s, grid)) !=
-        cudaSuccess)
-        return e;
+    // One accumulator buffer and three A stages pay for units of many stages
+    // (235B shape, 4,096 tokens, µs per layer-chunk: gate/up with K = 4096,
+    // 32 stages, 247.9 -> 237.8; down with K = 1536, 12 stages, a further ->
+    // 235.5), while with K = 2048 (16 stages) the lost epilogue overlap cost the
+    // 30B gate/up kernel more than the deeper A ring gave back (101.4 -> 102.6).
+    const bool one_gu = a.D / (kGpc * kKc) >= 20, one_dn = a.F / (kGpc * kKc) >= 12;
+    if (a.q2)
+        e = one_gu ? launch_tc<true, true, true, true>(mg, mu, mx, gu, s, grid)
+                   : launch_tc<true, true, true, false>(mg, mu, mx, gu, s, grid);
+    else
+        e = one_gu ? launch_tc<true, false, true, true>(mg, mu, mx, gu, s, grid)
+                   : launch_tc<true, false, true, false>(mg, mu, mx, gu, s, grid);
+    if (e != cudaSuccess) return e;
     TcParams dn = gu;
     dn.n_tiles = a.D / kTile;
     dn.n_chunks = a.F / kKc;
@@ -820,9 +837,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
         dn.s1 = a.ds + tile_groups;
         dn.b1 = a.db + tile_groups;
         dn.vec_scales = dn.vec_scales && a16(dn.s1) && a16(dn.b1);
-        return a.q2 ? launch_tc<true, true, false>(md, md, mh, dn, s, grid) : launch_tc<true, false, false>(md, md, mh, dn, s, grid);
+        if (a.q2)
+            return one_dn ? launch_tc<true, true, false, true>(md, md, mh, dn, s, grid)
+                          : launch_tc<true, true, false, false>(md, md, mh, dn, s, grid);
+        return one_dn ? launch_tc<true, false, false, true>(md, md, mh, dn, s, grid)
+                      : launch_tc<true, false, false, false>(md, md, mh, dn, s, grid);
     }
-    return a.q2 ? launch_tc<false, true, false>(md, md, mh, dn, s, grid) : launch_tc<false, false, false>(md, md, mh, dn, s, grid);
+    if (a.q2)
+        return one_dn ? launch_tc<false, true, false, true>(md, md, mh, dn, s, grid)
+                      : launch_tc<false, true, false, false>(md, md, mh, dn, s, grid);
+    return one_dn ? launch_tc<false, false, false, true>(md, md, mh, dn, s, grid)
+                  : launch_tc<false, false, false, false>(md, md, mh, dn, s, grid);
 }
 
 }  // namespace smoe
