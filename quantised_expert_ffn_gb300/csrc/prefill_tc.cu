@@ -536,8 +536,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (m == 0 && h == 0) {
                         // A stage a is free once the MMAs of stage g - kAS completed:
-                        // that stage's empty phase (it cannot have moved on since: stage
-                        // g + kAS is dequantised after this one)
+                        // that stage's empty phase (it cannot have moved on since: its
+                        // next phase needs the MMAs of stage g - kAS + kStages, which
+                        // run after this stage's)
                         if (g >= (uint32_t)kAS) {
                             const uint32_t gp = g - kAS;
                             if (!__all_sync(0xffffffffu, mbar_wait(&empty[gp % kStages], (gp / kStages) & 1, abort_flag, p.status)))
