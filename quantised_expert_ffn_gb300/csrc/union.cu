@@ -54,10 +54,25 @@ __global__ void __launch_bounds__(kUnionThreads) k_expert_union(UnionArgs a) {
     pdl_wait();
     pdl_launch_dependents();
 
-    for (int i = tid; i < E * kMaskWords; i += kUnionThreads) (&mask[0][0])[i] = 0ull;
+    // entries j = tid + 256 r, read once (N <= kMaxChunk * kMaxTopK = 4 * 256)
+    constexpr int kPer = kMaxChunk * kMaxTopK / kUnionThreads;
+    int ej[kPer];
+    float wj[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int j = tid + kUnionThreads * r;
+        ej[r] = j < N ? a.idx[j] : -1;
+        wj[r] = j < N ? a.w[j] : 0.f;
+    }
+    const int words = (N + 63) >> 6;            // mask words in use
+    for (int i = tid; i < E * kMaskWords; i += kUnionThreads)
+        if ((i % kMaskWords) < words) (&mask[0][0])[i] = 0ull;
     __syncthreads();
-    for (int j = tid; j < N; j += kUnionThreads) {
-        const int e = a.idx[j];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int j = tid + kUnionThreads * r;
+        if (j >= N) break;
+        const int e = ej[r];
         if (e >= 0 && e < E) atomicOr(&mask[e][j >> 6], 1ull << (j & 63));
         else set_status(a.status, SMOE_ERR_DEVICE);
     }
@@ -65,7 +80,7 @@ __global__ void __launch_bounds__(kUnionThreads) k_expert_union(UnionArgs a) {
 
     int cnt = 0;
     if (tid < E)
-        for (int q = 0; q < kMaskWords; ++q) cnt += __popcll(mask[tid][q]);
+        for (int q = 0; q < words; ++q) cnt += __popcll(mask[tid][q]);
     int ebase, epos, total, nu;
     scan2(cnt, cnt > 0 ? 1 : 0, ebase, epos, total, nu, wt);
     if (tid < E) base[tid] = ebase;
@@ -78,8 +93,11 @@ __global__ void __launch_bounds__(kUnionThreads) k_expert_union(UnionArgs a) {
     if (tid == 0) *a.n_union = nu;
     __syncthreads();
 
-    for (int j = tid; j < N; j += kUnionThreads) {
-        const int e = a.idx[j];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int j = tid + kUnionThreads * r;
+        if (j >= N) break;
+        const int e = ej[r];
         int pos = -1;
         if (e >= 0 && e < E) {
             pos = base[e];
@@ -88,7 +106,7 @@ __global__ void __launch_bounds__(kUnionThreads) k_expert_union(UnionArgs a) {
             pos += __popcll(mask[e][wq] & ((1ull << (j & 63)) - 1ull));
             a.bucket_tok[pos] = j / a.K;
             a.bucket_rank[pos] = j % a.K;
-            a.bucket_w[pos] = a.w[j];
+            a.bucket_w[pos] = wj[r];
         }
         if (a.slot_of) a.slot_of[j] = pos;
     }
