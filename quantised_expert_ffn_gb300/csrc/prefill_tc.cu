@@ -86,8 +86,8 @@ constexpr int kNmax = 64;
 // threads one commit per stage.  (The dequant warps release a stage's codes
 // only through that same barrier, after the MMAs: a TMA write may not follow
 // their reads of the same bytes without a proxy fence, and by then the values
-// read have long been consumed.)  Ring depths of 4 to 7 stages measure within
-// 3 % of each other.
+// read have long been consumed.)  Ring depths of 4 to 6 stages measure within
+// 3 % of each other; 7 (224 KB) are slower.
 constexpr int kGpc = 2;      // Q4 groups (64-code chunks along K) per stage
 constexpr int kStages = 6;
 constexpr int kAStages = 2;   // with two accumulator buffers; 3 with one (kOneAcc)
