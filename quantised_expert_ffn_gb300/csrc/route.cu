@@ -11,7 +11,7 @@
 // into shared memory, and each warp computes one router row (one expert) as a
 // warp-per-row dot product with 16-byte coalesced loads.  The last CTA of a
 // token to finish (device-scope ticket, no spinning) ranks the E logits and
-// writes the top-k ids and weights.
+// writes the top-k ids and weights (rank = the count of larger unique 64-bit keys).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kRouteThreads, 8) k_route_topk(RouteArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);               // [D] normed bf16
     __shared__ float red[kRouteWarps];
-    __shared__ uint32_t keys[kMaxExperts];
+    __shared__ __align__(16) unsigned long long keys[kMaxExperts];
     __shared__ float lsel[kMaxTopK];
     __shared__ int isel[kMaxTopK];
     __shared__ int am_last;
@@ -116,18 +116,24 @@ __global__ void __launch_bounds__(kRouteThreads, 8) k_route_topk(RouteArgs a) {
 
     const float *lg = a.logits + (size_t)t * E;
     float my = -INFINITY;
+    unsigned long long k0 = 0;
     if (tid < E) {
         my = __ldcg(lg + tid);
-        keys[tid] = order_key(my);
+        // unique key: the larger logit first, equal logits keep the lower id
+        k0 = ((unsigned long long)order_key(my) << 32) | (0xFFFFFFFFu - (uint32_t)tid);
+        keys[tid] = k0;
     }
     __syncthreads();
     if (tid < E) {
-        const uint32_t k0 = keys[tid];
-        int rank = 0;
-        for (int j = 0; j < E; ++j) {
-            const uint32_t kj = keys[j];
-            rank += (kj > k0) | ((kj == k0) & (j < tid));
+        int r0 = 0, r1 = 0;
+        const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(keys);
+        for (int j = 0; j < E / 2; ++j) {
+            const ulonglong2 kk = k2[j];
+            r0 += kk.x > k0;
+            r1 += kk.y > k0;
         }
+        if (E & 1) r0 += keys[E - 1] > k0;
+        const int rank = r0 + r1;
         if (rank < K) {
             isel[rank] = tid;
             lsel[rank] = my;
