@@ -7,7 +7,7 @@
 // on the GPU, as the pages' own horizon item ("The Dense Ceiling --
 // GPU-Resident Epilogue") proposes, and top-k stays on the GPU too.
 //
-// Grid (ceil(E / 8), T): a CTA of 8 warps normalises token t's hidden state
+// Grid (ceil(E / 16), T): a CTA of 16 warps normalises token t's hidden state
 // into shared memory, and each warp computes one router row (one expert) as a
 // warp-per-row dot product with 16-byte coalesced loads.  The last CTA of a
 // token to finish (device-scope ticket, no spinning) ranks the E logits and
@@ -19,7 +19,7 @@ namespace smoe {
 
 namespace {
 
-constexpr int kRouteWarps = 8;
+constexpr int kRouteWarps = 16;
 constexpr int kRouteThreads = kRouteWarps * 32;
 
 __device__ __forceinline__ float block_sum(float v, float *red) {
@@ -43,10 +43,10 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// At most 32 registers a thread, so 8 CTAs fit an SM and a 64-token chunk's
-// 1,024 CTAs run as one wave (at the 42 registers the code would otherwise
-// take, 5 per SM left a second wave).
-__global__ void __launch_bounds__(kRouteThreads, 8) k_route_topk(RouteArgs a) {
+// At most 32 registers a thread, so 4 CTAs of 512 threads fit an SM and a
+// 64-token chunk's 512 CTAs run as one wave (CTAs of 8 warps at the 42
+// registers the code would otherwise take left a second wave).
+__global__ void __launch_bounds__(kRouteThreads, 4) k_route_topk(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int D = a.D, E = a.E, K = a.K;
     const int t = blockIdx.y;
@@ -64,7 +64,21 @@ __global__ void __launch_bounds__(kRouteThreads, 8) k_route_topk(RouteArgs a) {
     const uint16_t *x = a.x + (size_t)t * D;
     // ---- RMSNorm (fp32) into shared memory ----
     if (a.gain) {
-        const float inv = block_rms_inv(x, D, a.eps, red);
+        // the reduction order of block_rms_inv (256 threads: stride-256 partials,
+        // a warp tree, the 8 warp sums in order), by the first 256 threads
+        float ss = 0.f;
+        if (tid < 256)
+            for (int d = tid; d < D; d += 256) {
+                const float v = bf16_to_f32(ld_cg_u16(x + d));
+                ss = fmaf(v, v, ss);
+            }
+        ss = warp_sum(ss);
+        if (lane == 0 && warp < 8) red[warp] = ss;
+        __syncthreads();
+        float tt = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tt += red[i];
+        const float inv = 1.0f / sqrtf(tt / (float)D + a.eps);
         for (int d = tid; d < D; d += kRouteThreads) xs[d] = rms_apply(x[d], inv, a.gain[d]);
     } else {
         for (int d = tid * 8; d < D; d += kRouteThreads * 8)
