@@ -24,7 +24,7 @@ size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for a layer shape and a token count.
 struct WsLayout {
     size_t status, counters, gbar, idx, w, logits, xn, xn16, h, n_union, union_ids, offsets,
-        bucket_tok, bucket_rank, bucket_w, slot_of, h32, hbuf, xperm, obuf, total;
+        bucket_tok, bucket_rank, bucket_w, slot_of, ready, h32, hbuf, xperm, obuf, total;
 };
 
 WsLayout ws_layout(const smoe_layer &L, int T) {
@@ -48,6 +48,7 @@ WsLayout ws_layout(const smoe_layer &L, int T) {
     o.bucket_rank = p; p = up(p + TK * 4);
     o.bucket_w = p;    p = up(p + TK * 4);
     o.slot_of = p;     p = up(p + TK * 4);
+    o.ready = p;       p = up(p + E * 4);
     o.h32 = p;         p = up(p + TK * F * 4);
     o.hbuf = p;        p = up(p + TK * F * 2);
     o.xperm = p;       p = up(p + TK * D * 2);
@@ -433,6 +434,7 @@ static int prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smo
     p.y = y;
     p.expert_out = expert_out;
     p.status = at<int32_t>(ws, o.status);
+    p.ready = at<int32_t>(ws, o.ready);
     p.num_sms = device_sm_count();
     p.q2 = is_q2(L) ? 1 : 0;
     if (tc) {

@@ -137,6 +137,7 @@ struct PrefillArgs {
     uint16_t *y;                // [T][D]
     float *expert_out;          // [T][K][D] unweighted o of each (token, rank), or NULL
     int32_t *status;
+    int32_t *ready;             // [E] gate/up -> down counters (tensor-core path), or NULL
     int num_sms;
     int q2;                     // 1: SMOE-Q2 codes (tensor-core path only)
 };

@@ -39,6 +39,12 @@
 //   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
+// The down kernel does not wait for the whole gate/up grid: each gate/up
+// epilogue warp counts its stored rows of h per union expert, and the down
+// kernel's TMA thread waits, per unit, for its expert's count to be complete,
+// so down CTAs start on the SMs that gate/up's last round of units leaves
+// idle (a dependent launch: it happens once every gate/up CTA runs, and no
+// gate/up CTA waits on down, so the waits always end).
 // TMEM: columns 0-255 two accumulator buffers (gate, up: 64 columns each), so
 // the epilogue of one unit overlaps the main loop of the next, and columns
 // 256-511 two stages of dequantised A (each two groups of both matrices); or,
@@ -113,6 +119,13 @@ struct TcParams {
     int vec_scales;         // K/64 % 8 == 0 and 16-byte aligned scale arrays: 8 groups per load
     __half *hout;           // gate/up: h [slots][F] fp16, K-permuted
     float *oout;            // down: o [slots][D] fp32
+    // Per union slot, the gate/up epilogue warps that have written their rows of
+    // h (each warp adds 1 once its 32 rows of a tile are stored).  Gate/up adds to
+    // it; down, with it set, waits per unit for ready_target instead of waiting
+    // for the whole gate/up grid, so its CTAs start on the SMs that gate/up's
+    // last round leaves idle.  NULL: neither.
+    int32_t *ready;
+    int ready_target;       // down: 4 warps x gate/up tiles per expert
     int32_t *status;
 };
 
@@ -163,6 +176,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile
     *abort_flag = 1;
     set_status(status, SMOE_ERR_TIMEOUT);
     return false;
+}
+
+// Bounded wait until *ctr >= target (gpu-scope acquire), then a proxy fence:
+// the bulk tensor reads issued after it see what the counter's writers
+// released.  On timeout it records SMOE_ERR_TIMEOUT and raises the CTA's abort
+// flag, as mbar_wait does.
+__device__ __forceinline__ bool wait_count(const int32_t *ctr, int target, volatile int *abort_flag,
+                                           int32_t *status) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v < target) {
+        const uint64_t t0 = global_ns();
+        while (true) {
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+            if (v >= target) break;
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                set_status(status, SMOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -386,10 +424,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    pdl_wait();                      // union, buckets and activations of the previous kernels
+    // The down kernel with ready counters waits per unit (see TcParams::ready)
+    // and for the previous grid only before it exits.  What else it reads was
+    // complete before any gate/up CTA passed its own wait, and its launch, a
+    // dependent one, happens only after every gate/up CTA has passed it; it
+    // reads the union through L2.
+    const bool overlap = !kHOut && p.ready != nullptr;
+    if (!overlap) pdl_wait();        // union, buckets and activations of the previous kernels
     pdl_launch_dependents();
 
-    const int nu = *p.n_union;
+    const int nu = __ldcg(p.n_union);
     const int n_units = nu * p.n_tiles;
     const int NC = p.n_chunks;
     const int NSC = NC / kGpc;       // stages per unit (K is a multiple of 128)
@@ -399,10 +443,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t g = 0;
             for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x) {
                 const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
-                const int e = p.union_ids[u];
-                const int off = p.offsets[u];
-                int m = p.offsets[u + 1] - off;
+                const int e = __ldcg(p.union_ids + u);
+                const int off = __ldcg(p.offsets + u);
+                int m = __ldcg(p.offsets + u + 1) - off;
                 m = m > kNmax ? kNmax : m;
+                if (overlap && !wait_count(p.ready + u, p.ready_target, abort_flag, p.status)) break;
                 const int nb = (m + 15) >> 4;            // 1..4
                 const CUtensorMap *tb = nb <= 1 ? &tm_b16 : nb == 2 ? &tm_b32 : nb == 3 ? &tm_b48 : &tm_b64;
                 const uint32_t bbytes = (uint32_t)(nb < 1 ? 1 : nb) * 16 * kKc * 2;  // full box, OOB rows zero-filled
@@ -432,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool issued = false;
             for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
                 const int u = unit / p.n_tiles;
-                int m = p.offsets[u + 1] - p.offsets[u];
+                int m = __ldcg(p.offsets + u + 1) - __ldcg(p.offsets + u);
                 m = m > kNmax ? kNmax : m;
                 const int npad = ((m + 15) >> 4) << 4;
                 const uint32_t idesc = idesc_f16(kTile, npad < 16 ? 16 : npad);
@@ -556,7 +601,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, gbase += NSC) {
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
-            const int e = p.union_ids[u];
+            const int e = __ldcg(p.union_ids + u);
             const size_t row = (size_t)e * p.rows_per_expert + tile * p.tile_rows + r;
             const int NG = p.k_dim / kGroup;
             bool ok = true;
@@ -630,8 +675,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t i = 0;
         for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
-            const int off = p.offsets[u];
-            int m = p.offsets[u + 1] - off;
+            const int off = __ldcg(p.offsets + u);
+            int m = __ldcg(p.offsets + u + 1) - off;
             if (m > kNmax) {
                 set_status(p.status, SMOE_ERR_DEVICE);
                 m = kNmax;
@@ -672,6 +717,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&accempty[b]);
+            if (kHOut && p.ready) {
+                // this warp's 32 rows of h for the unit are stored: count them
+                // (the stores ordered before the bulk tensor reads of the down kernel)
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.ready + u) : "memory");
+            }
         }
     }
 
@@ -683,6 +735,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
+    // the previous grid's completion is part of this one's (it has finished all
+    // its units by now: every one of them fed some down unit)
+    if (overlap) pdl_wait();
 }
 
 // Bucket-ordered, 8-block-permuted fp16 copy of the normed inputs:
@@ -690,6 +745,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 __global__ void __launch_bounds__(256) k_gather_xperm(PrefillArgs a) {
     pdl_wait();
     pdl_launch_dependents();
+    if (blockIdx.x == 0 && a.ready)   // the gate/up -> down counters start from zero
+        for (int i = threadIdx.x; i < a.E; i += blockDim.x) a.ready[i] = 0;
     const int s = blockIdx.x;
     const int total = a.offsets[*a.n_union];
     const int D = a.D;
@@ -802,6 +859,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     auto a16 = [](const void *q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
     gu.vec_scales = (a.D / kGroup) % 8 == 0 && a16(a.gs) && a16(a.gb) && a16(a.us) && a16(a.ub);
     gu.hout = a.hbuf;
+    gu.ready = a.ready;
     gu.status = a.status;
     // One accumulator buffer and three A stages pay for units of many stages
     // (235B shape, 4,096 tokens, µs per layer-chunk: gate/up with K = 4096,
@@ -828,6 +886,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     dn.vec_scales = (a.F / kGroup) % 8 == 0 && a16(a.ds) && a16(a.db);
     dn.hout = nullptr;
     dn.oout = a.obuf;
+    dn.ready_target = 4 * gu.n_tiles;
     if ((a.D / kTile) % 2 == 0) {
         // pairs of adjacent 128-row down tiles: each stage's activation tiles
         // feeds both, as gate and up share theirs
