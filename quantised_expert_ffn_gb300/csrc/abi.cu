@@ -24,7 +24,7 @@ size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for a layer shape and a token count.
 struct WsLayout {
     size_t status, counters, gbar, idx, w, logits, xn, xn16, h, n_union, union_ids, offsets,
-        bucket_tok, bucket_rank, bucket_w, slot_of, ready, h32, hbuf, xperm, obuf, total;
+        bucket_tok, bucket_rank, bucket_w, slot_of, ready, unit_ctr, h32, hbuf, xperm, obuf, total;
 };
 
 WsLayout ws_layout(const smoe_layer &L, int T) {
@@ -49,6 +49,7 @@ WsLayout ws_layout(const smoe_layer &L, int T) {
     o.bucket_w = p;    p = up(p + TK * 4);
     o.slot_of = p;     p = up(p + TK * 4);
     o.ready = p;       p = up(p + E * 4);
+    o.unit_ctr = p;    p = up(p + 2 * 4);
     o.h32 = p;         p = up(p + TK * F * 4);
     o.hbuf = p;        p = up(p + TK * F * 2);
     o.xperm = p;       p = up(p + TK * D * 2);
@@ -435,6 +436,7 @@ static int prefill_chunk(const smoe_layer *layer, const smoe_bf16 *x, int T, smo
     p.expert_out = expert_out;
     p.status = at<int32_t>(ws, o.status);
     p.ready = at<int32_t>(ws, o.ready);
+    p.unit_ctr = at<int32_t>(ws, o.unit_ctr);
     p.num_sms = device_sm_count();
     p.q2 = is_q2(L) ? 1 : 0;
     if (tc) {

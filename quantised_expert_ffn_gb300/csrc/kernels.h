@@ -138,6 +138,7 @@ struct PrefillArgs {
     float *expert_out;          // [T][K][D] unweighted o of each (token, rank), or NULL
     int32_t *status;
     int32_t *ready;             // [E] gate/up -> down counters (tensor-core path), or NULL
+    int32_t *unit_ctr;          // [2] gate/up and down unit counters (tensor-core path), or NULL
     int num_sms;
     int q2;                     // 1: SMOE-Q2 codes (tensor-core path only)
 };

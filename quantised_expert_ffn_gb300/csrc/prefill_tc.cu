@@ -10,7 +10,7 @@
 // tensor cores with the weights as the 128-row M side ("swap AB") and the
 // bucket's tokens as N (padded to a multiple of 16, at most 64).
 //
-// One persistent CTA per SM walks a static list of units (union expert u and
+// One persistent CTA per SM walks a list of units (union expert u and
 // its row tiles: a 128-row tile of both gate and up, or two adjacent 128-row
 // tiles of down, so that every stage of a unit feeds two MMA threads from one
 // set of activation tiles); per unit the K dimension is consumed in stages of
@@ -39,6 +39,10 @@
 //   warps 8-11  epilogue: tcgen05.ld the accumulator (each warp its 32 TMEM
 //               lanes = 32 weight rows) and write h = SiLU(g)*u as fp16
 //               (gate/up kernel) or the fp32 expert outputs (down kernel).
+// Units are handed out in order by a device counter: the TMA thread claims
+// the next one while it issues the current unit's last stages and posts it in
+// a small shared-memory queue that the other roles read, so a CTA that starts
+// late (a down CTA on an SM that gate/up freed late) or runs slow takes fewer.
 // The down kernel does not wait for the whole gate/up grid: each gate/up
 // epilogue warp counts its stored rows of h per union expert, and the down
 // kernel's TMA thread waits, per unit, for its expert's count to be complete,
@@ -98,6 +102,7 @@ constexpr int kGpc = 2;      // Q4 groups (64-code chunks along K) per stage
 constexpr int kStages = 6;
 constexpr int kAStages = 2;   // with two accumulator buffers; 3 with one (kOneAcc)
 constexpr uint32_t kTmemCols = 512;
+constexpr int kUQ = 4;       // unit queue entries: how many units the TMA thread may run ahead of the epilogue
 constexpr uint32_t kAccStride = 128;                  // two accumulator buffers: columns 0-127, 128-255
 constexpr uint32_t kUpCol = 64;                       // up accumulator after gate's (N <= 64 columns each)
 constexpr uint32_t kACol0 = 256;                      // A stages: columns 256-511 (128-511 with one buffer)
@@ -126,6 +131,10 @@ struct TcParams {
     // last round leaves idle.  NULL: neither.
     int32_t *ready;
     int ready_target;       // down: 4 warps x gate/up tiles per expert
+    // Units handed out in order by this counter (zero at launch), so a CTA that
+    // starts early or runs fast takes more of them; NULL: the static list
+    // blockIdx.x, + gridDim.x, ...
+    int32_t *unit_ctr;
     int32_t *status;
 };
 
@@ -392,6 +401,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *drain = accempty + 2;           // [2] all MMAs issued by MMA thread i complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // the unit queue: the TMA thread claims units from p.unit_ctr and posts
+    // them here in order; every consuming warp (or MMA thread) releases an entry
+    uint64_t *uq_full = reinterpret_cast<uint64_t *>(tmem_slot + 2);   // [kUQ]
+    uint64_t *uq_empty = uq_full + kUQ;                                 // [kUQ]
+    volatile int *uq = reinterpret_cast<volatile int *>(uq_empty + kUQ); // [kUQ] unit, -1: none left
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -410,6 +424,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
+        for (int i = 0; i < kUQ; ++i) {
+            mbar_init(&uq_full[i], 1);
+            mbar_init(&uq_empty[i], kProdThreads / 32 + 4 + kIssuers);   // dequant, epilogue warps, MMA threads
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -437,11 +455,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_units = nu * p.n_tiles;
     const int NC = p.n_chunks;
     const int NSC = NC / kGpc;       // stages per unit (K is a multiple of 128)
+    const bool dyn = p.unit_ctr != nullptr;
+    // The k-th unit of this CTA for a consuming warp (every lane returns it) or
+    // thread (lone = true): the static list, or the queue entry the TMA thread
+    // posted, released once read.  -1: no units left, or a wait gave up.
+    auto next_unit = [&](uint32_t k, bool lone) -> int {
+        if (!dyn) {
+            const int u = blockIdx.x + (int)k * (int)gridDim.x;
+            return u < n_units ? u : -1;
+        }
+        const int q = (int)(k % kUQ);
+        const bool got = mbar_wait(&uq_full[q], (k / kUQ) & 1, abort_flag, p.status);
+        if (lone) {
+            if (!got) return -1;
+            const int u = uq[q];
+            mbar_arrive(&uq_empty[q]);
+            return u;
+        }
+        if (!__all_sync(0xffffffffu, got)) return -1;
+        const int u = uq[q];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&uq_empty[q]);
+        return u;
+    };
 
     if (warp == kTmaWarp) {
         if (lane == 0) {
             uint32_t g = 0;
-            for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x) {
+            // dynamic: the next unit is claimed two stages before this unit's
+            // last, so the atomic's round trip overlaps the issue of those stages
+            int next = dyn ? atomicAdd(p.unit_ctr, 1) : -1;
+            const int claim_at = NSC > 2 ? NSC - 2 : 0;
+            for (uint32_t k = 0; !*abort_flag; ++k) {
+                int unit;
+                if (dyn) {
+                    unit = next < n_units ? next : -1;
+                    const int q = (int)(k % kUQ);
+                    if (k >= (uint32_t)kUQ && !mbar_wait(&uq_empty[q], ((k / kUQ) - 1) & 1, abort_flag, p.status)) break;
+                    uq[q] = unit;
+                    mbar_arrive(&uq_full[q]);
+                } else {
+                    unit = blockIdx.x + (int)k * (int)gridDim.x;
+                    if (unit >= n_units) unit = -1;
+                }
+                if (unit < 0) break;
                 const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
                 const int e = __ldcg(p.union_ids + u);
                 const int off = __ldcg(p.offsets + u);
@@ -453,6 +510,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t bbytes = (uint32_t)(nb < 1 ? 1 : nb) * 16 * kKc * 2;  // full box, OOB rows zero-filled
                 const int row = e * p.rows_per_expert + tile * p.tile_rows;
                 for (int c = 0; c < NSC; ++c, ++g) {
+                    if (dyn && c == claim_at) next = atomicAdd(p.unit_ctr, 1);
                     const int s = g % kStages;
                     const uint32_t ph = (g / kStages) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
@@ -475,7 +533,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0 && (mat == 0 || kPair)) {
             uint32_t g = 0, i = 0;
             bool issued = false;
-            for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
+            for (; !*abort_flag; ++i) {
+                const int unit = next_unit(i, true);
+                if (unit < 0) break;
                 const int u = unit / p.n_tiles;
                 int m = __ldcg(p.offsets + u + 1) - __ldcg(p.offsets + u);
                 m = m > kNmax ? kNmax : m;
@@ -599,7 +659,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(&afull[a]);
             return true;
         };
-        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, gbase += NSC) {
+        for (uint32_t k = 0; !*abort_flag; ++k, gbase += NSC) {
+            const int unit = next_unit(k, false);
+            if (unit < 0) break;
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
             const int e = __ldcg(p.union_ids + u);
             const size_t row = (size_t)e * p.rows_per_expert + tile * p.tile_rows + r;
@@ -672,8 +734,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---------------- epilogue (warps 8-11) ----------------
         const int q = warp - kEpiWarp0;                // TMEM lane quarter
         const int r = q * 32 + lane;                   // weight row in the tile
-        uint32_t i = 0;
-        for (int unit = blockIdx.x; unit < n_units && !*abort_flag; unit += gridDim.x, ++i) {
+        for (uint32_t i = 0; !*abort_flag; ++i) {
+            const int unit = next_unit(i, false);
+            if (unit < 0) break;
             const int u = unit / p.n_tiles, tile = unit - u * p.n_tiles;
             const int off = __ldcg(p.offsets + u);
             int m = __ldcg(p.offsets + u + 1) - off;
@@ -745,8 +808,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 __global__ void __launch_bounds__(256) k_gather_xperm(PrefillArgs a) {
     pdl_wait();
     pdl_launch_dependents();
-    if (blockIdx.x == 0 && a.ready)   // the gate/up -> down counters start from zero
+    if (blockIdx.x == 0 && a.ready) {  // the gate/up -> down counters and the unit counters start from zero
         for (int i = threadIdx.x; i < a.E; i += blockDim.x) a.ready[i] = 0;
+        if (threadIdx.x < 2 && a.unit_ctr) a.unit_ctr[threadIdx.x] = 0;
+    }
     const int s = blockIdx.x;
     const int total = a.offsets[*a.n_union];
     const int D = a.D;
@@ -860,6 +925,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     gu.vec_scales = (a.D / kGroup) % 8 == 0 && a16(a.gs) && a16(a.gb) && a16(a.us) && a16(a.ub);
     gu.hout = a.hbuf;
     gu.ready = a.ready;
+    gu.unit_ctr = a.unit_ctr;
     gu.status = a.status;
     // One accumulator buffer and three A stages pay for units of many stages
     // (235B shape, 4,096 tokens, µs per layer-chunk: gate/up with K = 4096,
@@ -887,6 +953,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     dn.hout = nullptr;
     dn.oout = a.obuf;
     dn.ready_target = 4 * gu.n_tiles;
+    dn.unit_ctr = a.unit_ctr ? a.unit_ctr + 1 : nullptr;
     if ((a.D / kTile) % 2 == 0) {
         // pairs of adjacent 128-row down tiles: each stage's activation tiles
         // feeds both, as gate and up share theirs
