@@ -930,11 +930,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     // One accumulator buffer and three A stages pay for units of many stages
     // (235B shape, 4,096 tokens, µs per layer-chunk: gate/up with K = 4096,
     // 32 stages, 247.9 -> 237.8; down with K = 1536, 12 stages, a further ->
-    // 235.5).  With units claimed from the counter they pay for the 30B gate/up
-    // kernel too (K = 2048, 16 stages: 95.4 -> 94.4; under the static unit list
-    // the lost epilogue overlap had cost more, 101.4 -> 102.6), but not for
-    // its down kernel (K = 768, 6 stages: no change).
-    const bool one_gu = a.D / (kGpc * kKc) >= 16, one_dn = a.F / (kGpc * kKc) >= 12;
+    // 235.5).  With units claimed from the counter they pay for the 30B SMOE-Q4
+    // gate/up kernel too (K = 2048, 16 stages: 95.4 -> 94.4; under the static
+    // unit list the lost epilogue overlap had cost more, 101.4 -> 102.6), but
+    // not for its down kernel (K = 768, 6 stages: no change) nor for SMOE-Q2,
+    // whose stages carry half the code bytes (30B prefill 19,468 -> 18,961 tok/s).
+    const bool one_gu = a.D / (kGpc * kKc) >= (a.q2 ? 20 : 16), one_dn = a.F / (kGpc * kKc) >= 12;
     if (a.q2)
         e = one_gu ? launch_tc<true, true, true, true>(mg, mu, mx, gu, s, grid)
                    : launch_tc<true, true, true, false>(mg, mu, mx, gu, s, grid);
