@@ -12,8 +12,9 @@ route alike (every bucket full), a ragged shape (6 and 10 groups: scales read
 group by group, an odd count of down tiles) and the largest layer taken;
 then weights written by the library's own
 quantiser (biases at the group minimum, not -8 s; some groups with scales
-below fp16's normal range) through decode and prefill; and the fp16 range
-bound of the tensor-core path."""
+below fp16's normal range) through decode and prefill; the fp16 range
+bound of the tensor-core path; and one chunk five times through the same
+workspace, bit-identical each time (units are claimed dynamically)."""
 import os
 
 import numpy as np
@@ -203,3 +204,35 @@ def test_prefill_reports_values_beyond_fp16(smoe, orc):
     # in range again: a clean workspace reads 0
     r3 = run_prefill(smoe, L2, bits(synth.hidden(4, D, seed=804)), 4, K, D)
     assert r3["status"] == 0
+
+
+@pytest.mark.parametrize("name,code_bits", [("235b", 4), ("30b", 4), ("30b", 2)])
+def test_prefill_repeats_bit_identical(smoe, orc, name, code_bits):
+    """The tensor-core kernels take their units from a device counter, so which
+    CTA computes which unit differs from call to call; each unit's arithmetic
+    does not depend on it.  The same chunk through the same workspace, five
+    times in a row: ids, weights, per-slot expert outputs and y equal bit for
+    bit every time, and the status word stays 0 (the counters are reset by
+    each call)."""
+    D, E, K, F = SHAPES[name]
+    W = synth.layer_weights(D, E, F, K, seed=900 + code_bits, device="cuda", rms_norm=True,
+                            code_bits=code_bits)
+    OL = oracle_layer(W)
+    L = smoe.Layer(W)
+    x = margin_tokens(OL, 64, seed=901, alpha=ALPHA[name])
+    ws = smoe.workspace(L, 64)
+    first = None
+    for _ in range(5):
+        y = torch.empty((64, D), dtype=torch.bfloat16, device="cuda")
+        idx = torch.empty((64, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((64, K), dtype=torch.float32, device="cuda")
+        eo = torch.full((64, K, D), float("nan"), dtype=torch.float32, device="cuda")
+        smoe.smoe_moe_prefill_chunk_experts(L, dev(x), 64, y, eo, idx, w, ws)
+        torch.cuda.synchronize()
+        assert smoe.smoe_read_device_status(ws) == 0
+        got = (host(idx), host(w).view(np.int32), host(eo).view(np.int32), host(y).view(np.int16))
+        if first is None:
+            first = got
+            continue
+        for a, b in zip(first, got):
+            assert np.array_equal(a, b)
